@@ -1,0 +1,368 @@
+"""Benchmark of the DCP sparse MLA decode hot path on one GB300 (or N replicas).
+
+A step is one fused decode launch (remap to owner shards, attention over every shard's
+paged FP8 KV, on-chip LSE merge) over the batch of the top-k-2048 / 128-head / FP8 KV
+workload: 64 sequences x 6 MTP query rows, 131072-token contexts, DCP = 8 token-
+interleaved shards.  The unfused pipeline (remap -> per-shard partials -> merge) is timed
+beside it.  Inputs are resident in HBM; L2 is flushed (256 MB write) between steps and
+each step is timed alone with CUDA events on the launching stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  --impl reference times the CPU oracle on a bounded sample of the
+same workload instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "sparse MLA decode rows/s + achieved HBM TB/s, top-k 2048, 128 heads, FP8 KV"
+WORKLOAD = "sparse MLA decode top-k 2048, 128 heads, FP8 E4M3 KV (per-128 scales), " \
+           "64 seqs x 6 MTP rows = 384 rows, context 131072, page 64, DCP=8 token-interleaved"
+BYTES_PER_SLOT = 656          # FP8 KV row gathered once per (row, selected slot)
+D_QK, D_V = 576, 512
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "src": "fallback"}
+
+
+class ClockSampler:
+    """SM clock and clock-event (throttle) reasons sampled every ~2 ms through NVML (read-only
+    queries via ctypes) in a background thread while the timed region runs; falls back to
+    nvidia-smi polling when NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev):
+        import ctypes
+        self.dev = dev
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self.nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(dev)
+            ok = False
+            if hasattr(props, "pci_bus_id"):
+                bus = ("%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                              getattr(props, "pci_device_id", 0))).encode()
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self.nvml, self.h, self.ct = nv, h, ctypes
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._reasons_fn = fn
+        except Exception:
+            self.nvml = None
+
+    def _run(self):
+        ct, nv, h = self.ct, self.nvml, self.h
+        mhz = ct.c_uint()
+        rs = ct.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0:
+                self.samples.append(float(mhz.value))
+            if self._reasons_fn(h, ct.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.002)
+
+    def start(self):
+        if self.nvml is not None:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+
+    def stop(self):
+        if self.nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["NVML unavailable"],
+                    "samples": 0}
+        self._stop.set()
+        self.t.join()
+        busy = self.samples
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(busy), "source": "nvml"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_workload(dev):
+    import synth
+    return synth.cfg3_sparse_topk2048_fp8(device=dev)
+
+
+def algorithmic(prob):
+    valid = int((prob.topk >= 0).sum().item())
+    return valid * BYTES_PER_SLOT, valid * 2.0 * prob.heads * (D_QK + D_V), valid
+
+
+def host_copy(prob):
+    """The same workload with every tensor in host memory (for the CPU oracle)."""
+    return prob.to("cpu")
+
+
+def time_oracle_rows(prob_host, budget_s):
+    """Oracle on as many rows of the workload as fit in about budget_s seconds."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.attention_problem(prob_host, rows=[0])
+    t1 = time.perf_counter() - t0
+    return max(1, min(prob_host.rows, int(budget_s / max(t1, 1e-4))))
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload per step."""
+    import oracle
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    prob = host_copy(make_workload(dev))
+    per_step = min(8.0, 150.0 / max(1, args.steps + args.warmup))
+    n = time_oracle_rows(prob, per_step)
+    rows = list(range(n))
+    for _ in range(args.warmup):
+        oracle.attention_problem(prob, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.attention_problem(prob, rows=rows)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    val = n * len(times) / total
+    cores = oracle.num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "rows/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rows_per_step": n, "parallelism": "cpu oracle"},
+            "cpu_baseline": {"value": val, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                             "sample": "%d of the 384 decode rows per step" % n},
+            "e2e": {"value": val, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_sample(prob):
+    """Oracle timed on host cores on a bounded sample of the same workload (rank 0, N = 1)."""
+    import oracle
+    host = host_copy(prob)
+    n = time_oracle_rows(host, 15.0)
+    t0 = time.perf_counter()
+    oracle.attention_problem(host, rows=list(range(n)))
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d of the 384 decode rows (2048 FP8 slots x 128 heads each), %.1f s"
+                      % (n, dt)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import decode_context_sparse_gb300 as dcp
+    from decode_context_sparse_gb300 import build
+    build.build()
+    dcp.load()
+
+    peaks = load_peaks()
+    prob = make_workload(dev)
+    kv_bytes, flops, valid = algorithmic(prob)
+    R = prob.rows
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    out = torch.empty((R, prob.heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, prob.heads), dtype=torch.float32, device=dev)
+
+    def step():
+        dcp.mla_decode_dcp_fused(prob.q, prob.pool, prob.kv_dtype, prob.block_table, prob.row_seq,
+                                 prob.sm_scale, prob.dcp, prob.interleave, idx=prob.topk,
+                                 out=out, lse=lse)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+
+    sampler = ClockSampler(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    sampler.start()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(times_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    avg_ms = total_ms / args.steps
+    value = ws * R * args.steps / (total_ms / 1e3)
+
+    # unfused pipeline (remap -> partials -> merge), same workload, same timing rules
+    D = prob.dcp
+    loc = torch.empty((D, R, prob.k), dtype=torch.int32, device=dev)
+    cnt = torch.empty((D, R), dtype=torch.int32, device=dev)
+    po = torch.empty((D, R, prob.heads, 512), dtype=torch.float32, device=dev)
+    pl = torch.empty((D, R, prob.heads), dtype=torch.float32, device=dev)
+
+    def unfused():
+        dcp.dcp_remap_topk(prob.topk, D, prob.interleave, local_idx=loc, count=cnt)
+        dcp.mla_decode_partial_lse(prob.q, prob.pool, prob.kv_dtype, prob.block_table,
+                                   prob.row_seq, prob.sm_scale, idx=loc, count=cnt, num_shards=D,
+                                   out=po, lse=pl)
+        dcp.dcp_lse_merge(po, pl, out=out, lse=lse)
+
+    for _ in range(3):
+        unfused()
+    uev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(max(3, args.steps // 2))]
+    for a, b in uev:
+        flush.fill_(1)
+        a.record(stream)
+        unfused()
+        b.record(stream)
+    torch.cuda.synchronize()
+    unfused_ms = statistics.mean(a.elapsed_time(b) for a, b in uev)
+
+    # end to end through the public API with host buffers: H2D of the step's inputs (queries,
+    # top-k ids, row map, block tables) from pinned memory, D2H of the outputs
+    h_q = prob.q.cpu().pin_memory()
+    h_topk = prob.topk.cpu().pin_memory()
+    h_rs = prob.row_seq.cpu().pin_memory()
+    h_bt = prob.block_table.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_topk = torch.empty_like(prob.q), torch.empty_like(prob.topk)
+    d_rs, d_bt = torch.empty_like(prob.row_seq), torch.empty_like(prob.block_table)
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_topk.copy_(h_topk, non_blocking=True)
+        d_rs.copy_(h_rs, non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        dcp.mla_decode_dcp_fused(d_q, prob.pool, prob.kv_dtype, d_bt, d_rs, prob.sm_scale,
+                                 prob.dcp, prob.interleave, idx=d_topk, out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(2)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_topk, h_rs, h_bt))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    e2e_val = ws * R * len(e2e_ms) / (sum(e2e_ms) / 1e3)
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    t_s = avg_ms / 1e3
+    hbm_tbs = kv_bytes / t_s / 1e12
+    tflops = flops / t_s / 1e12
+    t_hbm = kv_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": tflops / peaks["bf16_tflops"]}
+    else:
+        roof = {"bound": "hbm", "achieved": hbm_tbs * 1e3, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": hbm_tbs * 1e3 / peaks["hbm_gbs"]}
+    roof["traffic"] = None
+    roof["peak_src"] = peaks["src"]
+    roof["kernel"] = "mla_decode_dcp_fused"
+    roof["roofline_us"] = 1e6 * max(t_hbm, t_tc)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": avg_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": os.environ.get("DCP_BENCH_DTYPE", "f32"),
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": R, "heads": prob.heads, "topk": prob.k,
+                   "dcp": prob.dcp, "interleave": prob.interleave, "context": 131072,
+                   "kv_dtype": "fp8_e4m3_per128_scale", "l2": "flushed between steps (256 MB write)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "achieved_hbm_tbs": hbm_tbs,
+        "achieved_tflops": tflops,
+        "tokens_per_s": value,
+        "kv_slots_gathered_per_s": ws * valid * args.steps / (total_ms / 1e3),
+        "us_per_layer": 1e3 * avg_ms,
+        "unfused": {"ms_per_step": unfused_ms, "rows_per_s": R / (unfused_ms / 1e3),
+                    "launches_per_step": 3},
+        "roofline": roof,
+        "clocks": clocks,
+        "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+        "gpu_launches": args.steps,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(prob)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+// extern "C" entry points of libdcpmla: host-side argument checks, path choice and
+// launches on the caller's stream.  No allocation, no synchronisation.
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace dcp;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? DCP_OK : DCP_ERR_CUDA; }
+
+bool valid_rule(int32_t dcp, int32_t interleave) {
+  return dcp >= 1 && dcp <= DCP_MAX_SHARDS && interleave >= 1 && interleave <= (1 << 16);
+}
+
+// Common checks of a decode call; fills the device params (no workspace binding).
+int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t dcp,
+                   int32_t interleave, DecodeParams& p, bool& sparse) {
+  if (a == nullptr) return DCP_ERR_INVALID_ARG;
+  if (a->rows < 0 || n < 1 || n > DCP_MAX_SHARDS) return DCP_ERR_INVALID_ARG;
+  if (fused && !valid_rule(dcp, interleave)) return DCP_ERR_INVALID_ARG;
+  if (!a->q || !a->kv_pool || !a->block_table || !a->row_seq || !a->out || !a->lse)
+    return DCP_ERR_INVALID_ARG;
+  if (!aligned(a->q, 16) || !aligned(a->kv_pool, 16) || !aligned(a->out, 16) ||
+      !aligned(a->lse, 4))
+    return DCP_ERR_INVALID_ARG;
+  if (a->num_pages < 1 || a->num_seqs < 1 || a->bt_stride < 1) return DCP_ERR_INVALID_ARG;
+  if (a->kv_dtype != DCP_KV_BF16 && a->kv_dtype != DCP_KV_FP8_E4M3_S128)
+    return DCP_ERR_UNSUPPORTED;
+  if (a->heads < kSimtHeadGroup || a->heads > 128 || a->heads % kSimtHeadGroup != 0)
+    return DCP_ERR_UNSUPPORTED;
+  if (a->page_size != 64) return DCP_ERR_UNSUPPORTED;
+  if (!(a->sm_scale == a->sm_scale)) return DCP_ERR_INVALID_ARG;  // NaN
+  sparse = a->idx != nullptr;
+  if (sparse) {
+    if (a->k < 1 || a->k > DCP_MAX_TOPK) return DCP_ERR_INVALID_ARG;
+    if (!fused && a->count == nullptr) return DCP_ERR_INVALID_ARG;
+  } else {
+    if (a->kv_len == nullptr || a->max_kv_len < 0) return DCP_ERR_INVALID_ARG;
+  }
+  if (a->num_splits < 0) return DCP_ERR_INVALID_ARG;
+  const int64_t units = fused ? a->rows : a->rows * n;
+  const int64_t max_tokens = sparse ? a->k : a->max_kv_len;
+  int splits = a->num_splits > 0 ? a->num_splits : simt_auto_splits(units, a->heads, max_tokens);
+  if (splits > 64) splits = 64;
+
+  p.q = a->q;
+  p.rows = a->rows;
+  p.heads = a->heads;
+  p.scale_log2 = a->sm_scale * kLog2e;
+  p.pool = static_cast<const uint8_t*>(a->kv_pool);
+  p.num_pages = a->num_pages;
+  p.page_size = a->page_size;
+  p.bt = a->block_table;
+  p.num_seqs = a->num_seqs;
+  p.bt_stride = a->bt_stride;
+  p.row_seq = a->row_seq;
+  p.idx = a->idx;
+  p.count = a->count;
+  p.k = a->k;
+  p.kv_len = a->kv_len;
+  p.D = fused ? dcp : 1;
+  p.I = fused ? interleave : 1;
+  p.num_units = units;
+  p.num_splits = splits;
+  p.out = a->out;
+  p.lse = a->lse;
+  p.ws_o = nullptr;
+  p.ws_lse = nullptr;
+  p.ws_cnt = nullptr;
+  p.err = a->checked ? a->err_flag : nullptr;
+  return DCP_OK;
+}
+
+int bind_workspace(const dcp_mla_decode_args* a, DecodeParams& p) {
+  const size_t need = simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
+  if (need == 0) return DCP_OK;
+  if (a->workspace == nullptr || a->workspace_bytes < need || !aligned(a->workspace, 256))
+    return DCP_ERR_WORKSPACE;
+  simt_bind_workspace(p, a->workspace);
+  return DCP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dcp_status_string(int status) {
+  switch (status) {
+    case DCP_OK: return "DCP_OK";
+    case DCP_ERR_INVALID_ARG: return "DCP_ERR_INVALID_ARG: invalid argument";
+    case DCP_ERR_UNSUPPORTED: return "DCP_ERR_UNSUPPORTED: unsupported configuration";
+    case DCP_ERR_CUDA: return "DCP_ERR_CUDA: a CUDA call or launch failed";
+    case DCP_ERR_WORKSPACE: return "DCP_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    default: return "unknown dcp_status";
+  }
+}
+
+int dcp_abi_version(void) { return DCP_ABI_VERSION; }
+
+int dcp_remap_topk(const int32_t* global_idx, int64_t rows, int32_t k, int32_t dcp,
+                   int32_t interleave, int32_t shard, int32_t* local_idx, int32_t* count,
+                   dcp_stream_t stream) {
+  if (!global_idx || !local_idx || !count) return DCP_ERR_INVALID_ARG;
+  if (rows < 0 || rows > INT32_MAX || k < 1 || k > DCP_MAX_TOPK) return DCP_ERR_INVALID_ARG;
+  if (!valid_rule(dcp, interleave) || shard < -1 || shard >= dcp) return DCP_ERR_INVALID_ARG;
+  return status_of(launch_remap_topk(global_idx, rows, k, dcp, interleave, shard, local_idx, count,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dcp_local_lengths(const int32_t* global_len, int64_t rows, int32_t dcp, int32_t interleave,
+                      int32_t shard, int32_t* local_len, dcp_stream_t stream) {
+  if (!global_len || !local_len || rows < 0) return DCP_ERR_INVALID_ARG;
+  if (!valid_rule(dcp, interleave) || shard < -1 || shard >= dcp) return DCP_ERR_INVALID_ARG;
+  return status_of(launch_local_lengths(global_len, rows, dcp, interleave, shard, local_len,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dcp_lse_merge(const float* part_out, const float* part_lse, int32_t dcp, int64_t rows,
+                  int32_t heads, int32_t dv, void* out, float* lse, dcp_stream_t stream) {
+  if (!part_out || !part_lse || !out || !lse) return DCP_ERR_INVALID_ARG;
+  if (dcp < 1 || dcp > DCP_MAX_SHARDS || rows < 0 || heads < 1 || dv < 4 || dv % 4 != 0)
+    return DCP_ERR_INVALID_ARG;
+  if (!aligned(part_out, 16) || !aligned(out, 8) || !aligned(part_lse, 4) || !aligned(lse, 4))
+    return DCP_ERR_INVALID_ARG;
+  return status_of(launch_lse_merge(part_out, part_lse, dcp, rows, heads, dv, out, lse,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t mla_decode_workspace_size(const dcp_mla_decode_args* args, int32_t num_shards_or_dcp,
+                                 int32_t fused) {
+  DecodeParams p;
+  bool sparse;
+  const int32_t d = num_shards_or_dcp;
+  if (prepare_decode(args, fused ? 1 : d, fused != 0, d, 1, p, sparse) != DCP_OK)
+    return (size_t)-1;
+  return simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
+}
+
+int mla_decode_partial_lse(const dcp_mla_decode_args* args, int32_t num_shards,
+                           dcp_stream_t stream) {
+  DecodeParams p;
+  bool sparse;
+  int rc = prepare_decode(args, num_shards, false, 1, 1, p, sparse);
+  if (rc != DCP_OK) return rc;
+  if ((rc = bind_workspace(args, p)) != DCP_OK) return rc;
+  return status_of(launch_decode_simt(p, args->kv_dtype, false, sparse,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t interleave,
+                         dcp_stream_t stream) {
+  DecodeParams p;
+  bool sparse;
+  int rc = prepare_decode(args, 1, true, dcp, interleave, p, sparse);
+  if (rc != DCP_OK) return rc;
+  if ((rc = bind_workspace(args, p)) != DCP_OK) return rc;
+  return status_of(launch_decode_simt(p, args->kv_dtype, true, sparse,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Internal launchers of libdcpmla (host side; not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dcp {
+
+// Device-side view of one decode call (partial or fused).
+struct DecodeParams {
+  const void* q;          // [rows][heads][576] bf16
+  int64_t rows;
+  int heads;
+  float scale_log2;       // sm_scale * log2(e): logits are kept in base-2 units
+  const uint8_t* pool;
+  int64_t num_pages;
+  int page_size;
+  const int32_t* bt;      // partial: [shards][seqs][stride]; fused: [D][seqs][stride]
+  int num_seqs;
+  int bt_stride;
+  const int32_t* row_seq;
+  const int32_t* idx;     // sparse ids (local for partial, global for fused) or NULL
+  const int32_t* count;   // partial sparse counts
+  int k;
+  const int32_t* kv_len;  // dense lengths (local for partial, global for fused)
+  int D, I;               // fused: owner rule
+  int64_t num_units;      // partial: shards * rows; fused: rows
+  int num_splits;
+  void* out;              // partial: fp32 [units][H][512]; fused: bf16 [rows][H][512]
+  float* lse;
+  float* ws_o;            // split partials [units][splits][H][512]
+  float* ws_lse;          // [units][splits][H]
+  unsigned* ws_cnt;       // tickets [units][head groups]
+  int32_t* err;           // optional error word
+};
+
+cudaError_t launch_remap_topk(const int32_t* gidx, int64_t rows, int k, int D, int I, int shard,
+                              int32_t* local_idx, int32_t* count, cudaStream_t st);
+cudaError_t launch_local_lengths(const int32_t* glen, int64_t rows, int D, int I, int shard,
+                                 int32_t* llen, cudaStream_t st);
+cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int D, int64_t rows,
+                             int heads, int dv, void* out, float* lse, cudaStream_t st);
+
+// SIMT decode (any head count that is a multiple of 16).
+constexpr int kSimtHeadGroup = 16;
+size_t simt_workspace_bytes(int64_t units, int heads, int splits);
+int simt_auto_splits(int64_t units, int heads, int64_t max_tokens);
+void simt_bind_workspace(DecodeParams& p, void* ws);
+cudaError_t launch_decode_simt(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,
+                               cudaStream_t st);
+
+}  // namespace dcp

@@ -1,0 +1,220 @@
+/*
+ * dcpmla.h -- C ABI of libdcpmla.so, the GB300 (sm_103a) hot path of decode context
+ * parallelism (DCP) for MLA and DeepSeek-style sparse attention (DSA) decode.
+ *
+ * DCP shards the KV tokens of every sequence across D shards; each decode row attends
+ * to every shard's local KV and the shard results are merged with log-sum-exp weights
+ * (LMDeploy PR #4952 "support decode context parallelism for PyTorch MLA", Summary).
+ * On one GPU the shards are partitions of one paged KV pool in that GPU's HBM.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked (device) are CUDA device pointers; (host) are host pointers.
+ *     The caller allocates, owns and frees every buffer.  The library never allocates,
+ *     frees or synchronises; inputs are never written.
+ *   - Every call is asynchronous on `stream` (NULL = legacy default stream).  A return
+ *     of DCP_OK means the work was queued; kernel-side findings go to err_flag.
+ *   - Host-side argument checks run before any launch; a failed check returns a
+ *     negative dcp_status and launches nothing.  A failed launch returns DCP_ERR_CUDA.
+ *   - No kernel traps, asserts or waits without bound.
+ *
+ * Token row layout of the paged KV pool (a page is page_size consecutive token rows):
+ *   DCP_KV_BF16          : 576 bf16 (latent 0..511, RoPE 512..575)              1152 B
+ *   DCP_KV_FP8_E4M3_S128 : 512 e4m3 latent | 4 fp32 scales (one per 128 latent
+ *                          values, value = e4m3 * scale) | 64 bf16 RoPE          656 B
+ * Keys are the whole 576-value row; values are its first 512 values (MLA latent).
+ *
+ * Owner rule (DCP interleave): global slot t of a sequence lives on shard
+ *   (t / I) % D at local slot (t / (I*D))*I + t % I,
+ * with I = 1 (token-interleaved, "slot mod D") or I = page_size (page-interleaved,
+ * "page mod D").  A shard keeps its slots of a sequence in increasing global order.
+ */
+#ifndef DCPMLA_H
+#define DCPMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (struct CUstream_st*); declared here so that this
+ * header does not need the CUDA headers. */
+typedef struct CUstream_st* dcp_stream_t;
+
+typedef enum {
+  DCP_OK = 0,
+  DCP_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer */
+  DCP_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. head count) */
+  DCP_ERR_CUDA = -3,         /* a CUDA call or launch failed */
+  DCP_ERR_WORKSPACE = -4     /* workspace missing or smaller than required */
+} dcp_status;
+
+typedef enum {
+  DCP_KV_BF16 = 0,
+  DCP_KV_FP8_E4M3_S128 = 1
+} dcp_kv_dtype;
+
+/* Bits a kernel ORs into *err_flag (only when err_flag != NULL and checked != 0). */
+#define DCP_ERRBIT_SLOT_RANGE 1   /* a slot id past the block table row, or negative local id */
+#define DCP_ERRBIT_PAGE_RANGE 2   /* a block-table entry outside [0, num_pages) */
+
+#define DCP_MAX_SHARDS 64
+#define DCP_MAX_TOPK 16384
+
+/* Human-readable text for a dcp_status value (static storage). */
+const char* dcp_status_string(int status);
+
+/* ABI version of this header (bumped on any incompatible change). */
+#define DCP_ABI_VERSION 1
+int dcp_abi_version(void);
+
+/*
+ * dcp_remap_topk -- per-shard slot remap of DSA top-k indices.
+ * Passage: SGLang PR #42536 "Fix DCP for RoPE sparse attention on Blackwell",
+ *   Modifications, "Index remap": take the global top-k slots, keep the ones the shard
+ *   owns, convert them to local slot ids, move them to the front of the row and return
+ *   the count per row.
+ *
+ * global_idx (device) [rows][k] int32: global slot ids; any negative entry is padding.
+ * dcp        number of shards D, 1..DCP_MAX_SHARDS.
+ * interleave I >= 1 of the owner rule (1 or the page size).
+ * shard      -1: produce every shard; 0..D-1: produce only that shard.
+ * local_idx  (device) [n_out][rows][k] int32, n_out = D (shard = -1) or 1: for shard s
+ *            the local ids of the owned slots in their original order, then -1.
+ * count      (device) [n_out][rows] int32: number of owned slots of each row.
+ * Exact integer work; results are bit-identical to the definition.
+ * Errors: DCP_ERR_INVALID_ARG for null pointers, rows < 0, k < 1 or > DCP_MAX_TOPK,
+ *   dcp out of range, interleave < 1, shard outside [-1, D).  rows = 0 is a no-op.
+ */
+int dcp_remap_topk(const int32_t* global_idx, int64_t rows, int32_t k, int32_t dcp,
+                   int32_t interleave, int32_t shard, int32_t* local_idx, int32_t* count,
+                   dcp_stream_t stream);
+
+/*
+ * dcp_local_lengths -- local KV length of each row on one shard for dense decode.
+ * Passage: LMDeploy PR #4952, Summary (KV tokens are sharded across ranks; decode
+ *   attends to the local KV); a row of visible global length L holds, on shard s, the
+ *   slots t < L with owner s.
+ * global_len (device) [rows] int32 >= 0; local_len (device) [n_out][rows] int32 with
+ * n_out = D (shard = -1) or 1.  Errors as dcp_remap_topk.
+ */
+int dcp_local_lengths(const int32_t* global_len, int64_t rows, int32_t dcp,
+                      int32_t interleave, int32_t shard, int32_t* local_len,
+                      dcp_stream_t stream);
+
+/*
+ * Arguments of the decode entry points.  Field meaning differs between the per-shard
+ * call (mla_decode_partial_lse) and the fused call (mla_decode_dcp_fused) where noted.
+ */
+typedef struct {
+  /* queries */
+  const void* q;               /* (device) [rows][heads][576] bf16, 16-B aligned */
+  int64_t rows;                /* decode rows (query tokens), >= 0 */
+  int32_t heads;               /* query heads per row: a multiple of 16, 16..128 */
+  float sm_scale;              /* softmax scale applied to q.k before exp */
+  /* paged KV pool shared by all shards */
+  const void* kv_pool;         /* (device) [num_pages][page_size][token bytes], 16-B aligned */
+  int64_t num_pages;
+  int32_t kv_dtype;            /* dcp_kv_dtype */
+  int32_t page_size;           /* tokens per page: 64 */
+  /* block tables: partial call: [num_shards][num_seqs][bt_stride] starting at the
+   * first shard of the call; fused call: [dcp][num_seqs][bt_stride].  Entry j of a
+   * (shard, sequence) row is the physical page holding local slots
+   * j*page_size .. j*page_size+page_size-1. */
+  const int32_t* block_table;  /* (device) */
+  int32_t num_seqs;
+  int32_t bt_stride;           /* entries per (shard, sequence) row */
+  const int32_t* row_seq;      /* (device) [rows] sequence index of each row */
+  /* token selection: sparse when idx != NULL, dense otherwise */
+  const int32_t* idx;          /* (device) partial: [num_shards][rows][k] local ids as
+                                  produced by dcp_remap_topk (valid ids first);
+                                  fused: [rows][k] global ids, negatives = padding */
+  const int32_t* count;        /* (device) partial sparse: [num_shards][rows] valid ids;
+                                  fused: unused (NULL) */
+  int32_t k;                   /* top-k row length, 1..DCP_MAX_TOPK (sparse) */
+  const int32_t* kv_len;       /* (device) dense: partial: [num_shards][rows] local
+                                  lengths (dcp_local_lengths); fused: [rows] visible
+                                  global lengths */
+  int32_t max_kv_len;          /* dense: an upper bound of kv_len (sizes the split-KV
+                                  grid and the workspace); sparse: ignored */
+  /* outputs */
+  void* out;                   /* (device) partial: [num_shards][rows][heads][512] fp32;
+                                  fused: [rows][heads][512] bf16 */
+  float* lse;                  /* (device) partial: [num_shards][rows][heads];
+                                  fused: [rows][heads]; natural log; -inf = no KV */
+  /* scratch */
+  void* workspace;             /* (device) >= mla_decode_workspace_size() bytes, 256-B
+                                  aligned, all zero before its first use; every call
+                                  leaves it ready for the next (no clearing needed).
+                                  Calls that share a workspace must not overlap. */
+  size_t workspace_bytes;
+  int32_t num_splits;          /* split-KV factor per row: 0 = library choice */
+  /* diagnostics */
+  int32_t checked;             /* != 0: bounds-check every slot and page id */
+  int32_t* err_flag;           /* (device, optional) DCP_ERRBIT_* ORed in when checked */
+} dcp_mla_decode_args;
+
+/*
+ * mla_decode_partial_lse -- MLA decode attention over one or more shards' local KV,
+ * returning the shard output and its log-sum-exp.
+ * Passage: SGLang PR #42536, Modifications, "Backend": sparse attention is called with
+ *   return_lse=True and rows that have no local KV are fixed up; LMDeploy PR #4952,
+ *   Summary: attend to local KV (dense or sparse MLA, BF16 KV and sparse-MLA FP8 KV).
+ * For each shard s of the call, row r, head h over the shard's slot set S (sparse: the
+ * first count[s][r] local ids of idx[s][r]; dense: local slots 0..kv_len[s][r]-1):
+ *   logit_t = sm_scale * q[r][h] . key_t (576 values),  lse = ln sum_t exp(logit_t),
+ *   out[s][r][h] = sum_t exp(logit_t - lse) * key_t[0:512];
+ * an empty S gives out = 0 and lse = -inf (the fix-up).  Arithmetic: BF16 or exact
+ * E4M3->BF16 operands, FP32 accumulation; FP8 scales applied in FP32.
+ * num_shards: shards in this call (1..DCP_MAX_SHARDS); arrays are strided by shard.
+ * Errors: DCP_ERR_INVALID_ARG (null/misaligned pointers, bad sizes),
+ *   DCP_ERR_UNSUPPORTED (heads, page size, dtype), DCP_ERR_WORKSPACE, DCP_ERR_CUDA.
+ */
+int mla_decode_partial_lse(const dcp_mla_decode_args* args, int32_t num_shards,
+                           dcp_stream_t stream);
+
+/*
+ * dcp_lse_merge -- merge shard partials with LSE weights.
+ * Passage: LMDeploy PR #4952, Summary ("merge outputs using LSE weights") and its
+ *   review discussion (merge arithmetic in FP32, merged result stored in BF16);
+ *   SGLang PR #36990 "DCP for DSA models with the flashmla_kv backend", review of the
+ *   LSE combine, and SGLang PR #42536, Modifications, "Fixes in shared code": when every
+ *   shard is empty the result is a zero output and a -inf LSE, not 0/0.
+ *   m = max_s lse_s;  m = -inf -> out = 0, lse = -inf;
+ *   else w_s = exp(lse_s - m), W = sum_s w_s, out = sum_s w_s out_s / W, lse = m + ln W.
+ * part_out (device) [dcp][rows][heads][dv] fp32; part_lse (device) [dcp][rows][heads];
+ * out (device) [rows][heads][dv] bf16; lse (device) [rows][heads] fp32.
+ * dv: a multiple of 4 (512 for MLA).  Pointers 16-B aligned.
+ */
+int dcp_lse_merge(const float* part_out, const float* part_lse, int32_t dcp, int64_t rows,
+                  int32_t heads, int32_t dv, void* out, float* lse, dcp_stream_t stream);
+
+/*
+ * mla_decode_dcp_fused -- the whole DCP decode of a row in one launch: for every
+ * global slot of the row, read the key row from its owner shard's pages, attend, and
+ * merge across shards on chip; the result equals unsharded attention.
+ * Passage: SGLang PR #42536, Follow-ups #1: a fused merge kernel in place of the three
+ *   per-layer merge kernels (pack, exchange, LSE combine) is the biggest remaining
+ *   latency item; this is its single-GPU form (all shards of a row in one launch).
+ * args: fused meanings (global idx or global kv_len, [dcp] block tables, bf16 out).
+ * Split-KV partials of a row are merged by the last CTA to finish (an atomic ticket in
+ * the workspace; no waiting).  Errors as mla_decode_partial_lse.
+ */
+int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t interleave,
+                         dcp_stream_t stream);
+
+/*
+ * mla_decode_workspace_size -- bytes of workspace a decode call with these arguments
+ * needs (0 when none).  fused = 0 for mla_decode_partial_lse (num_shards_or_dcp =
+ * num_shards), 1 for mla_decode_dcp_fused (num_shards_or_dcp = dcp).  Returns
+ * (size_t)-1 for invalid arguments.
+ */
+size_t mla_decode_workspace_size(const dcp_mla_decode_args* args, int32_t num_shards_or_dcp,
+                                 int32_t fused);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCPMLA_H */

@@ -1,0 +1,107 @@
+"""The C-ABI library loads, exports every symbol include/dcpmla.h declares, and rejects
+invalid arguments on the host before any launch (these calls touch no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dcpmla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_context_sparse_gb300 import build
+    build.build()
+    import decode_context_sparse_gb300 as dcp
+    return dcp.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                       src, flags=re.M)
+    return sorted(set(n for n in names if not n.startswith("defined")))
+
+
+def test_header_declares_the_four_path_entry_points():
+    names = declared_functions()
+    for n in ("dcp_remap_topk", "mla_decode_partial_lse", "dcp_lse_merge", "mla_decode_dcp_fused"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import decode_context_sparse_gb300 as dcp
+    names = declared_functions()
+    assert sorted(dcp.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    import decode_context_sparse_gb300 as dcp
+    assert lib.dcp_abi_version() == dcp.DCP_ABI_VERSION
+    for st in (0, -1, -2, -3, -4):
+        assert lib.dcp_status_string(st).decode().startswith("DCP_")
+    assert b"unknown" in lib.dcp_status_string(7)
+
+
+def test_remap_rejects_bad_arguments(lib):
+    good = ctypes.c_void_p(256)
+    call = lib.dcp_remap_topk
+    assert call(None, 4, 8, 2, 1, -1, good, good, None) == -1          # null input
+    assert call(good, 4, 0, 2, 1, -1, good, good, None) == -1          # k < 1
+    assert call(good, 4, 1 << 20, 2, 1, -1, good, good, None) == -1    # k too large
+    assert call(good, 4, 8, 0, 1, -1, good, good, None) == -1          # dcp < 1
+    assert call(good, 4, 8, 65, 1, -1, good, good, None) == -1         # dcp too large
+    assert call(good, 4, 8, 2, 0, -1, good, good, None) == -1          # interleave < 1
+    assert call(good, 4, 8, 2, 1, 2, good, good, None) == -1           # shard >= dcp
+    assert call(good, -1, 8, 2, 1, -1, good, good, None) == -1         # rows < 0
+
+
+def test_merge_rejects_bad_arguments(lib):
+    g = ctypes.c_void_p(4096)
+    call = lib.dcp_lse_merge
+    assert call(None, g, 2, 4, 8, 512, g, g, None) == -1
+    assert call(g, g, 0, 4, 8, 512, g, g, None) == -1
+    assert call(g, g, 2, 4, 8, 510, g, g, None) == -1                  # dv % 4
+    assert call(ctypes.c_void_p(4100), g, 2, 4, 8, 512, g, g, None) == -1  # misaligned
+
+
+def _args(**kw):
+    import decode_context_sparse_gb300 as dcp
+    a = dcp.DecodeArgs()
+    p = 1 << 20
+    a.q = p; a.rows = 4; a.heads = 128; a.sm_scale = 0.07
+    a.kv_pool = p; a.num_pages = 10; a.kv_dtype = 1; a.page_size = 64
+    a.block_table = p; a.num_seqs = 2; a.bt_stride = 4; a.row_seq = p
+    a.idx = p; a.count = p; a.k = 2048
+    a.out = p; a.lse = p
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_decode_rejects_bad_arguments(lib):
+    import decode_context_sparse_gb300 as dcp
+    part, fused = lib.mla_decode_partial_lse, lib.mla_decode_dcp_fused
+    R = ctypes.byref
+    assert part(R(_args(q=None)), 1, None) == dcp.DCP_ERR_INVALID_ARG
+    assert part(R(_args(q=(1 << 20) + 2)), 1, None) == dcp.DCP_ERR_INVALID_ARG   # misaligned q
+    assert part(R(_args(heads=100)), 1, None) == dcp.DCP_ERR_UNSUPPORTED
+    assert part(R(_args(heads=256)), 1, None) == dcp.DCP_ERR_UNSUPPORTED
+    assert part(R(_args(page_size=16)), 1, None) == dcp.DCP_ERR_UNSUPPORTED
+    assert part(R(_args(kv_dtype=5)), 1, None) == dcp.DCP_ERR_UNSUPPORTED
+    assert part(R(_args(k=0)), 1, None) == dcp.DCP_ERR_INVALID_ARG
+    assert part(R(_args(count=None)), 1, None) == dcp.DCP_ERR_INVALID_ARG      # sparse partial
+    assert part(R(_args()), 0, None) == dcp.DCP_ERR_INVALID_ARG                # no shards
+    assert part(R(_args(idx=None)), 1, None) == dcp.DCP_ERR_INVALID_ARG        # dense w/o kv_len
+    assert fused(R(_args()), 0, 1, None) == dcp.DCP_ERR_INVALID_ARG
+    assert fused(R(_args()), 8, 0, None) == dcp.DCP_ERR_INVALID_ARG
+    # a split-KV call without workspace is refused before launch
+    assert fused(R(_args(num_splits=4)), 8, 1, None) == dcp.DCP_ERR_WORKSPACE
+    assert lib.mla_decode_workspace_size(R(_args(num_splits=4)), 8, 1) > 0
+    assert lib.mla_decode_workspace_size(R(_args(q=None)), 8, 1) == ctypes.c_size_t(-1).value
+    assert lib.mla_decode_workspace_size(R(_args(num_splits=1)), 8, 1) == 0
