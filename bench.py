@@ -116,9 +116,9 @@ def dist_env():
     return ws, rank, local
 
 
-def make_workload(dev):
+def make_workload(dev, seqs=64):
     import synth
-    return synth.cfg3_sparse_topk2048_fp8(device=dev)
+    return synth.cfg3_sparse_topk2048_fp8(device=dev, seqs=seqs)
 
 
 def algorithmic(prob):
@@ -194,6 +194,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=64,
+                    help="sequences of the workload (64 = the full workload; fewer only for "
+                         "profiling captures that must stay small)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -210,7 +213,7 @@ def main():
     dcp.load()
 
     peaks = load_peaks()
-    prob = make_workload(dev)
+    prob = make_workload(dev, args.seqs)
     kv_bytes, flops, valid = algorithmic(prob)
     R = prob.rows
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

@@ -76,13 +76,16 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   return DCP_OK;
 }
 
-int bind_workspace(const dcp_mla_decode_args* a, DecodeParams& p) {
+// Binds the caller's workspace and clears the split tickets with an asynchronous memset on
+// the call's stream, so a workspace may be shared by calls of different shapes.
+int bind_workspace(const dcp_mla_decode_args* a, DecodeParams& p, cudaStream_t st) {
   const size_t need = simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
   if (need == 0) return DCP_OK;
   if (a->workspace == nullptr || a->workspace_bytes < need || !aligned(a->workspace, 256))
     return DCP_ERR_WORKSPACE;
   simt_bind_workspace(p, a->workspace);
-  return DCP_OK;
+  const size_t nbytes = (size_t)p.num_units * (p.heads / kSimtHeadGroup) * sizeof(unsigned);
+  return status_of(cudaMemsetAsync(p.ws_cnt, 0, nbytes, st));
 }
 
 }  // namespace
@@ -147,9 +150,9 @@ int mla_decode_partial_lse(const dcp_mla_decode_args* args, int32_t num_shards,
   bool sparse;
   int rc = prepare_decode(args, num_shards, false, 1, 1, p, sparse);
   if (rc != DCP_OK) return rc;
-  if ((rc = bind_workspace(args, p)) != DCP_OK) return rc;
-  return status_of(launch_decode_simt(p, args->kv_dtype, false, sparse,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = bind_workspace(args, p, st)) != DCP_OK) return rc;
+  return status_of(launch_decode_simt(p, args->kv_dtype, false, sparse, st));
 }
 
 int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t interleave,
@@ -158,9 +161,9 @@ int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t i
   bool sparse;
   int rc = prepare_decode(args, 1, true, dcp, interleave, p, sparse);
   if (rc != DCP_OK) return rc;
-  if ((rc = bind_workspace(args, p)) != DCP_OK) return rc;
-  return status_of(launch_decode_simt(p, args->kv_dtype, true, sparse,
-                                      reinterpret_cast<cudaStream_t>(stream)));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = bind_workspace(args, p, st)) != DCP_OK) return rc;
+  return status_of(launch_decode_simt(p, args->kv_dtype, true, sparse, st));
 }
 
 }  // extern "C"

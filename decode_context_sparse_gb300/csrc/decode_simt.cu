@@ -24,10 +24,6 @@ constexpr int kTile = 32;
 constexpr int kKStride = 580;  // fp32 row stride of the K tile: float4 reads conflict-free
 constexpr int kHG = kSimtHeadGroup;
 
-struct TokenRef {
-  const uint8_t* row;  // NULL = masked slot
-};
-
 // Resolve position `pos` of unit (row r, shard s) to a pool row; NULL when it is padding
 // or out of range (reported through err when given).
 template <bool FUSED, bool SPARSE>
@@ -321,7 +317,6 @@ decode_simt_kernel(const DecodeParams p) {
     }
     if (lane == 0) p.lse[unit * H + h0 + h] = lse_out;
   }
-  if (tid == 0) p.ws_cnt[unit * (H / kHG) + hg] = 0u;  // ready for the next call
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

@@ -145,9 +145,10 @@ typedef struct {
                                   fused: [rows][heads]; natural log; -inf = no KV */
   /* scratch */
   void* workspace;             /* (device) >= mla_decode_workspace_size() bytes, 256-B
-                                  aligned, all zero before its first use; every call
-                                  leaves it ready for the next (no clearing needed).
-                                  Calls that share a workspace must not overlap. */
+                                  aligned; its contents need not persist between calls
+                                  (a call clears what it uses with an asynchronous
+                                  memset on its stream).  Calls that share a workspace
+                                  must not overlap on the GPU. */
   size_t workspace_bytes;
   int32_t num_splits;          /* split-KV factor per row: 0 = library choice */
   /* diagnostics */

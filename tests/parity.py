@@ -3,9 +3,11 @@ the two GPU pipelines (unfused remap -> partial -> merge, and the fused launch).
 import numpy as np
 import torch
 
-# Tolerances of the path (floating point): outputs max abs error <= 1e-2 and max relative
-# error <= 2e-2 where |ref| >= 0.5 (where a relative error is meaningful); LSE max abs
-# error <= 1e-3 on finite entries, -inf must match exactly.  Remap is bit-exact.
+# Tolerances of the path (floating point): an output element passes when its error is
+# within 1e-2 absolute or 2e-2 relative to the reference, i.e. err <= max(1e-2, 2e-2*|ref|)
+# (abs bound for small values, rel bound for large ones: BF16 storage alone rounds a value
+# in [4, 8) by up to 0.0156).  LSE max abs error <= 1e-3 on finite entries, -inf must match
+# exactly.  Remap is bit-exact.
 OUT_ATOL = 1e-2
 OUT_RTOL = 2e-2
 REL_FLOOR = 0.5
@@ -23,11 +25,11 @@ def check_out(got, ref, what=""):
     assert g.shape == r.shape, (what, g.shape, r.shape)
     assert np.isfinite(g).all(), "%s: non-finite output" % what
     err = np.abs(g - r)
-    assert err.max(initial=0.0) <= OUT_ATOL, "%s: max abs err %.3g" % (what, err.max())
-    big = np.abs(r) >= REL_FLOOR
-    if big.any():
-        rel = (err[big] / np.abs(r[big])).max()
-        assert rel <= OUT_RTOL, "%s: max rel err %.3g" % (what, rel)
+    allowed = np.maximum(OUT_ATOL, OUT_RTOL * np.abs(r))
+    worst = (err / allowed).max(initial=0.0)
+    small = np.abs(r) < REL_FLOOR
+    assert worst <= 1.0, "%s: error %.3g of allowed (max abs err %.3g on |ref|<0.5: %.3g)" % (
+        what, worst, err.max(), err[small].max(initial=0.0))
     return float(err.max(initial=0.0))
 
 
