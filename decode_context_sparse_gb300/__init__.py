@@ -34,7 +34,8 @@ TOKEN_BYTES = {DCP_KV_BF16: 1152, DCP_KV_FP8_E4M3_S128: 656}
 # every symbol include/dcpmla.h declares
 EXPORTS = ("dcp_status_string", "dcp_abi_version", "dcp_remap_topk", "dcp_local_lengths",
            "mla_decode_partial_lse", "dcp_lse_merge", "mla_decode_dcp_fused",
-           "mla_decode_workspace_size")
+           "mla_decode_workspace_size", "mla_decode_dcp_fused_noalloc")
+DCP_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class DcpError(RuntimeError):
@@ -88,6 +89,8 @@ def load(path: str = LIB_PATH):
     lib.dcp_lse_merge.argtypes = [V, V, I32, I64, I32, I32, V, V, V]
     lib.mla_decode_dcp_fused.restype = ctypes.c_int
     lib.mla_decode_dcp_fused.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32, V]
+    lib.mla_decode_dcp_fused_noalloc.restype = ctypes.c_int
+    lib.mla_decode_dcp_fused_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32, V]
     lib.mla_decode_workspace_size.restype = SZ
     lib.mla_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32]
     if lib.dcp_abi_version() != DCP_ABI_VERSION:
@@ -282,4 +285,24 @@ def mla_decode_dcp_fused(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, d
     _bind_ws(a, dcp, True, q.device, workspace)
     _check(load().mla_decode_dcp_fused(ctypes.byref(a), dcp, interleave, _stream(stream)),
            "mla_decode_dcp_fused")
+    return out, lse
+
+
+def mla_decode_dcp_fused_noalloc(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, dcp,
+                                 interleave, *, out, lse, idx=None, kv_len=None, max_kv_len=None,
+                                 num_splits=0, checked=False, err_flag=None, stream=None):
+    """mla_decode_dcp_fused for callers that cannot allocate device memory.
+
+    The caller passes preallocated outputs (out [R,H,512] bf16, lse [R,H] fp32); neither this
+    function nor the library allocates anything: the split-KV scratch is a fixed
+    DCP_NOALLOC_SCRATCH_BYTES array inside the library, shared by every call on a device.
+    The first call on a device looks the array up, so make it before any stream capture;
+    calls that overlap on the GPU race on the array.  A call that would need more scratch
+    raises DcpError(DCP_ERR_WORKSPACE)."""
+    if max_kv_len is None and kv_len is not None:
+        raise ValueError("dense calls must pass max_kv_len (reading it from kv_len would sync)")
+    a = _decode_args(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx, None, kv_len,
+                     max_kv_len, out, lse, num_splits, checked, err_flag)
+    _check(load().mla_decode_dcp_fused_noalloc(ctypes.byref(a), dcp, interleave, _stream(stream)),
+           "mla_decode_dcp_fused_noalloc (static scratch %d bytes)" % DCP_NOALLOC_SCRATCH_BYTES)
     return out, lse

@@ -17,6 +17,10 @@ bool valid_rule(int32_t dcp, int32_t interleave) {
   return dcp >= 1 && dcp <= DCP_MAX_SHARDS && interleave >= 1 && interleave <= (1 << 16);
 }
 
+}  // namespace
+
+namespace dcp {
+
 // Common checks of a decode call; fills the device params (no workspace binding).
 int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t dcp,
                    int32_t interleave, DecodeParams& p, bool& sparse) {
@@ -75,6 +79,10 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   p.err = a->checked ? a->err_flag : nullptr;
   return DCP_OK;
 }
+
+}  // namespace dcp
+
+namespace {
 
 // Binds the caller's workspace and clears the split tickets with an asynchronous memset on
 // the call's stream, so a workspace may be shared by calls of different shapes.

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/dcpmla.h"
+
 namespace dcp {
 
 // Device-side view of one decode call (partial or fused).
@@ -49,5 +51,9 @@ int simt_auto_splits(int64_t units, int heads, int64_t max_tokens);
 void simt_bind_workspace(DecodeParams& p, void* ws);
 cudaError_t launch_decode_simt(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,
                                cudaStream_t st);
+
+// Host-side checks shared by the decode entry points; fills p (workspace not bound).
+int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t dcp,
+                   int32_t interleave, DecodeParams& p, bool& sparse);
 
 }  // namespace dcp

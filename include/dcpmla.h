@@ -206,6 +206,31 @@ int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t i
                          dcp_stream_t stream);
 
 /*
+ * mla_decode_dcp_fused_noalloc -- mla_decode_dcp_fused for callers that cannot
+ * allocate device memory.  This entry point has no counterpart on the pages; it exists
+ * for integration.  Some callers are handed only their inputs and outputs by a host
+ * runtime that owns all device memory (a plugin or custom op inside another inference
+ * engine, a serving loop that reserves its memory once at start-up, a step recorded
+ * into a CUDA graph), and a cudaMalloc there is refused, breaks the capture or stalls
+ * the device, so they cannot supply the split-KV workspace.
+ * Same arguments and results as mla_decode_dcp_fused; args->workspace and
+ * args->workspace_bytes are ignored.  The scratch is a static device array of
+ * DCP_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that loads it until
+ * the process exits.  The call allocates and frees nothing.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - A call whose split-KV scratch would exceed DCP_NOALLOC_SCRATCH_BYTES
+ *     (rows * splits * heads * 2 KB plus small tables) returns DCP_ERR_WORKSPACE and
+ *     launches nothing; lower num_splits or the rows per call.
+ *   - All calls share the array and it keeps the last call's contents; each call clears
+ *     the tickets it needs with an asynchronous memset on its stream.  Calls that overlap
+ *     on the GPU (different streams or host threads) race on the array.
+ */
+#define DCP_NOALLOC_SCRATCH_BYTES (16u << 20)
+int mla_decode_dcp_fused_noalloc(const dcp_mla_decode_args* args, int32_t dcp,
+                                 int32_t interleave, dcp_stream_t stream);
+
+/*
  * mla_decode_workspace_size -- bytes of workspace a decode call with these arguments
  * needs (0 when none).  fused = 0 for mla_decode_partial_lse (num_shards_or_dcp =
  * num_shards), 1 for mla_decode_dcp_fused (num_shards_or_dcp = dcp).  Returns
