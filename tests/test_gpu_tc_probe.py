@@ -1,0 +1,64 @@
+"""Probe of the tcgen05 building blocks (TMEM A operand, K-major and MN-major SW128 B
+operands, shared-memory A operand) against torch matmul, and of the exact E4M3 -> bf16
+conversion used by the FP8 tensor-core path."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "tc_probe.cu")
+SO = os.path.join(HERE, "..", "_build", "libtc_probe.so")
+
+
+@pytest.fixture(scope="module")
+def probe():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    os.makedirs(os.path.dirname(SO), exist_ok=True)
+    subprocess.check_call(["/usr/local/cuda/bin/nvcc", "-gencode", "arch=compute_103a,code=sm_103a",
+                           "-O2", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", SRC, "-o", SO])
+    lib = ctypes.CDLL(SO)
+    lib.tc_probe.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    lib.e4m3_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    return lib
+
+
+def _run(lib, A, B, K, N, mode):
+    D = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert lib.tc_probe(A.data_ptr(), B.data_ptr(), D.data_ptr(), K, N, mode, err.data_ptr()) == 0
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    return D
+
+
+@pytest.mark.parametrize("mode,K,N", [(0, 64, 16), (0, 64, 32), (0, 128, 64), (0, 128, 256),
+                                      (2, 64, 16), (2, 128, 128),
+                                      (1, 16, 128), (1, 32, 64), (1, 32, 256), (1, 128, 256)])
+def test_mma_layouts(probe, mode, K, N):
+    g = torch.Generator(device="cuda").manual_seed(K * 1000 + N + mode)
+    A = torch.randn((128, K), generator=g, device="cuda").to(torch.bfloat16)
+    if mode == 1:
+        B = torch.randn((K, N), generator=g, device="cuda").to(torch.bfloat16)
+        ref = A.float() @ B.float()
+    else:
+        B = torch.randn((N, K), generator=g, device="cuda").to(torch.bfloat16)
+        ref = A.float() @ B.float().t()
+    D = _run(probe, A, B, K, N, mode)
+    assert torch.allclose(D, ref, atol=1e-3, rtol=1e-4), (D - ref).abs().max().item()
+
+
+def test_e4m3_to_bf16_exact(probe):
+    codes = torch.arange(65536, dtype=torch.int32).to(torch.int16).to("cuda")
+    out = torch.empty(65536, dtype=torch.int32, device="cuda")
+    assert probe.e4m3_probe(codes.data_ptr(), out.data_ptr(), 65536) == 0
+    torch.cuda.synchronize()
+    got = out.view(torch.bfloat16).float().view(65536, 2).double() * 2.0 ** 112
+    b = codes.view(torch.uint8).view(65536, 2)
+    ref = b.view(torch.float8_e4m3fn).double()
+    finite = ~torch.isnan(ref)
+    assert torch.equal(got[finite], ref[finite])
