@@ -26,6 +26,7 @@ DCP_KV_BF16 = 0
 DCP_KV_FP8_E4M3_S128 = 1
 DCP_ERRBIT_SLOT_RANGE = 1
 DCP_ERRBIT_PAGE_RANGE = 2
+DCP_ERRBIT_TIMEOUT = 4
 DCP_MAX_SHARDS = 64
 DCP_MAX_TOPK = 16384
 DCP_ABI_VERSION = 1

@@ -77,6 +77,16 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   p.ws_lse = nullptr;
   p.ws_cnt = nullptr;
   p.err = a->checked ? a->err_flag : nullptr;
+  // tensor-core path for 48..128 heads (rows of up to 128 heads, padded)
+  p.use_tc = (tc_path_enabled() && a->heads > 32) ? 1 : 0;
+  p.pairs = 0;
+  p.tc_o = p.tc_l = nullptr;
+  p.tc_cnt = nullptr;
+  p.err_timeout = a->err_flag;  // timeouts are reported whenever err_flag is given
+  if (p.use_tc) {
+    const int tn = tc_tile_slots(a->kv_dtype);
+    p.pairs = tc_pairs_for(units, units * ((max_tokens + tn - 1) / tn));
+  }
   return DCP_OK;
 }
 
@@ -87,6 +97,13 @@ namespace {
 // Binds the caller's workspace and clears the split tickets with an asynchronous memset on
 // the call's stream, so a workspace may be shared by calls of different shapes.
 int bind_workspace(const dcp_mla_decode_args* a, DecodeParams& p, cudaStream_t st) {
+  if (p.use_tc) {
+    const size_t need = tc_workspace_bytes(p.num_units, p.pairs);
+    if (a->workspace == nullptr || a->workspace_bytes < need || !aligned(a->workspace, 256))
+      return DCP_ERR_WORKSPACE;
+    tc_bind_workspace(p, a->workspace);
+    return status_of(cudaMemsetAsync(p.tc_cnt, 0, tc_ticket_bytes(p.num_units), st));
+  }
   const size_t need = simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
   if (need == 0) return DCP_OK;
   if (a->workspace == nullptr || a->workspace_bytes < need || !aligned(a->workspace, 256))
@@ -149,6 +166,7 @@ size_t mla_decode_workspace_size(const dcp_mla_decode_args* args, int32_t num_sh
   const int32_t d = num_shards_or_dcp;
   if (prepare_decode(args, fused ? 1 : d, fused != 0, d, 1, p, sparse) != DCP_OK)
     return (size_t)-1;
+  if (p.use_tc) return tc_workspace_bytes(p.num_units, p.pairs);
   return simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
 }
 
@@ -160,7 +178,9 @@ int mla_decode_partial_lse(const dcp_mla_decode_args* args, int32_t num_shards,
   if (rc != DCP_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = bind_workspace(args, p, st)) != DCP_OK) return rc;
-  return status_of(launch_decode_simt(p, args->kv_dtype, false, sparse, st));
+  if (p.num_units == 0) return DCP_OK;
+  return status_of(p.use_tc ? launch_decode_tc(p, args->kv_dtype, false, sparse, st)
+                            : launch_decode_simt(p, args->kv_dtype, false, sparse, st));
 }
 
 int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t interleave,
@@ -171,7 +191,9 @@ int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t i
   if (rc != DCP_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if ((rc = bind_workspace(args, p, st)) != DCP_OK) return rc;
-  return status_of(launch_decode_simt(p, args->kv_dtype, true, sparse, st));
+  if (p.num_units == 0) return DCP_OK;
+  return status_of(p.use_tc ? launch_decode_tc(p, args->kv_dtype, true, sparse, st)
+                            : launch_decode_simt(p, args->kv_dtype, true, sparse, st));
 }
 
 }  // extern "C"

@@ -1,0 +1,907 @@
+// Tensor-core (tcgen05 / TMEM) MLA decode attention with LSE for 48..128 heads, BF16 or
+// FP8-E4M3 (per-128 scale) latent KV: the per-shard partial form and the fused
+// all-shards form.  What it computes is the same as the CUDA-core path
+// (LMDeploy PR #4952 "support decode context parallelism for PyTorch MLA", Summary;
+// SGLang PR #42536 "Fix DCP for RoPE sparse attention on Blackwell", Modifications,
+// "Backend"; Follow-ups #1).
+//
+// Why two CTAs per row.  With 128 heads the output accumulator O[128 heads x 512] fp32
+// alone fills the 512 TMEM columns of an SM.  A cluster of two CTAs therefore shares
+// each row: CTA c owns latent dims [256c, 256c+256) and RoPE dims [512+32c, 512+32c+32)
+// of every key, computes the partial logits q.k over its 288 dims and the output columns
+// of its 256 value dims.  The two partial logit tiles are exchanged through distributed
+// shared memory (st.async counted on the peer's mbarrier), both CTAs run the same
+// softmax, and neither ever loads a KV byte the other loads.
+//
+// Per CTA (384 threads):
+//   warp 0      producer: resolves slot -> owner shard -> page and bulk-copies this CTA's
+//               share of each KV row (latent half, RoPE half, FP8 scales) into a staging
+//               ring (cp.async.bulk, completion counted in bytes);
+//   warp 1      TMEM owner and MMA issuer (one thread): S = Q K^T with Q as the A operand
+//               in TMEM, then O += P V with P as the A operand in TMEM;
+//   warps 4-7   converters: staging -> SWIZZLE_128B bf16 K tile (FP8: E4M3 -> bf16 times
+//               2^-112, exact), zero rows for padding, tile metadata (mask, scales);
+//   warps 8-11  softmax: thread h owns head h (TMEM lane h): reads its logits, exchanges
+//               partial logits with the peer, online softmax in base 2 with a lazily
+//               raised reference max (the output is rescaled only when the max grows by
+//               more than 2^8), writes P as bf16 into TMEM, and at the end of a row
+//               normalises O and writes it out (or merges split rows).
+// TMEM columns: O [0,256) | Q [256,400) | two logit buffers from 400 (FP8: three
+// accumulators per buffer -- latent block lo, latent block hi, RoPE -- since the FP8
+// scales differ per 128-block; BF16: one); P overwrites its logit buffer after the read.
+//
+// FP8 numerics: the latent lives in shared memory as exact bf16 images of e4m3 * 2^-112;
+// each 128-block's partial logit is scaled in fp32 by (scale * 2^56) * 2^56, so the
+// logits carry fp32 accuracy; for P V the block scale is folded into P (P * scale * 2^56
+// in bf16) and O is multiplied by 2^56 at the end.
+//
+// Work: a persistent grid of pairs; the concatenated sequence of 16/32-slot tiles of all
+// units (rows, or (shard, row) pairs) is cut into equal contiguous ranges, one per pair.
+// A unit cut by a range edge leaves fp32 partials in the workspace; the last pair to
+// finish it (atomic ticket, no waiting) merges them.  Every wait is bounded; a wait that
+// expires sets an abort flag, the CTA winds down and DCP_ERRBIT_TIMEOUT is reported.
+#include <stdlib.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace dcp {
+using namespace tc;
+
+template <int KVT>
+struct TcCfg;
+template <>
+struct TcCfg<DCP_KV_FP8_E4M3_S128> {
+  static constexpr int TN = 16, NACC = 3, NS = 4, NK = 3, STG_LAT = 256, STG_SC = 16;
+  static constexpr int ROW_LAT = 256, ROW_ROPE = 528, ROW_SC = 512;  // byte offsets in a row
+};
+template <>
+struct TcCfg<DCP_KV_BF16> {
+  static constexpr int TN = 32, NACC = 1, NS = 3, NK = 3, STG_LAT = 512, STG_SC = 0;
+  static constexpr int ROW_LAT = 512, ROW_ROPE = 1024, ROW_SC = 0;
+};
+
+constexpr int kTcThreads = 384;
+constexpr int kColO = 0, kColQ = 256, kColS = 400;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kTwo56 = 72057594037927936.0f;  // 2^56
+
+template <int KVT>
+struct TcLay {
+  using C = TcCfg<KVT>;
+  static constexpr int TN = C::TN;
+  static constexpr int BS = TN * 128;  // bytes between 64-dim column blocks of a K tile
+  static constexpr int KT_BYTES = 5 * BS;
+  static constexpr int STG_TOK = C::STG_LAT + 64 + C::STG_SC;
+  static constexpr int STG_BYTES = TN * STG_TOK;
+  static constexpr int XSTRIDE = TN + 4;  // floats per exchange row (16-B aligned rows)
+  static constexpr int X_BYTES = 128 * XSTRIDE * 4;
+  static constexpr int META_BYTES = 16 + TN * 8;
+  static constexpr int SBUF = C::NACC * TN;
+  static constexpr int OFF_KT = 0;
+  static constexpr int OFF_STG = OFF_KT + C::NK * KT_BYTES;
+  static constexpr int OFF_X = OFF_STG + C::NS * STG_BYTES;
+  static constexpr int OFF_META = OFF_X + 2 * X_BYTES;
+  static constexpr int OFF_END = OFF_META + C::NK * META_BYTES;
+  // at least 120 KB so that one CTA (and one TMEM owner) sits on an SM
+  static constexpr int SMEM = (OFF_END + 1024 > 122880 ? OFF_END + 1024 : 122880);
+};
+
+struct TcShared {
+  uint64_t stg_full[4], stg_empty[4], kt_full[3], kt_empty[3];
+  uint64_t s_full[2], p_full[2], pv_done, q_ready, in_full[2], out_free[2], drain;
+  uint64_t x_read[2];         // all softmax threads have read inbox x
+  uint64_t fin_pub, fin_dec;  // split-unit publish / merge decision
+  uint32_t stg_mask[4];
+  uint32_t tmem_base;
+  int abort_flag;
+  int last_flag;
+  int64_t T, t0;
+  int Peff;  // pairs that own tiles: min(pairs, T), so no pair's range is empty
+  int64_t unit0;
+  int tile0, ntiles;
+  int64_t scan_base;
+  int64_t warp_sum[12];
+};
+
+struct UnitInfo {
+  int64_t r;
+  int shard, b, n, ntile;
+};
+
+template <bool FUSED, bool SPARSE, int TN>
+__device__ __forceinline__ UnitInfo get_unit(const DecodeParams& p, int64_t u) {
+  UnitInfo x;
+  x.r = FUSED ? u : u % p.rows;
+  x.shard = FUSED ? 0 : (int)(u / p.rows);
+  x.b = __ldg(p.row_seq + x.r);
+  if (SPARSE)
+    x.n = FUSED ? p.k : min(max(__ldg(p.count + u), 0), p.k);
+  else
+    x.n = max(0, __ldg(p.kv_len + u));
+  if (x.b < 0 || x.b >= p.num_seqs) x.n = 0;
+  x.ntile = (x.n + TN - 1) / TN;
+  return x;
+}
+
+// Walk over this pair's tiles, unit by unit (empty units contribute no tiles).
+template <bool FUSED, bool SPARSE, int TN>
+struct Walk {
+  int64_t u;
+  int lt, left;
+  UnitInfo info;
+  __device__ void init(const DecodeParams& p, int64_t u0, int tile0, int ntiles) {
+    u = u0;
+    lt = tile0;
+    left = ntiles;
+    if (left > 0) info = get_unit<FUSED, SPARSE, TN>(p, u);
+  }
+  __device__ bool first() const { return lt == 0; }
+  __device__ bool last() const { return lt == info.ntile - 1; }
+  __device__ void next(const DecodeParams& p) {
+    if (--left <= 0) return;
+    if (++lt == info.ntile) {
+      do {
+        ++u;
+        info = get_unit<FUSED, SPARSE, TN>(p, u);
+      } while (info.ntile == 0);
+      lt = 0;
+    }
+  }
+};
+
+// Global pool row of token position `pos` of the unit, or nullptr (padding / out of range).
+template <int KVT, bool FUSED, bool SPARSE>
+__device__ __forceinline__ const uint8_t* tc_resolve(const DecodeParams& p, const UnitInfo& x,
+                                                     int64_t u, int pos) {
+  if (pos >= x.n) return nullptr;
+  int l;
+  const int32_t* table;
+  if (FUSED) {
+    const int t = SPARSE ? __ldg(p.idx + x.r * (int64_t)p.k + pos) : pos;
+    if (t < 0) return nullptr;
+    const int s = owner_of(t, p.D, p.I);
+    l = local_of(t, p.D, p.I);
+    table = p.bt + ((int64_t)s * p.num_seqs + x.b) * p.bt_stride;
+  } else {
+    l = SPARSE ? __ldg(p.idx + u * (int64_t)p.k + pos) : pos;
+    if (l < 0) {
+      set_err(p.err, DCP_ERRBIT_SLOT_RANGE);
+      return nullptr;
+    }
+    table = p.bt + ((int64_t)x.shard * p.num_seqs + x.b) * p.bt_stride;
+  }
+  const int pj = l >> 6;  // page size 64
+  if (pj >= p.bt_stride) {
+    set_err(p.err, DCP_ERRBIT_SLOT_RANGE);
+    return nullptr;
+  }
+  const int page = __ldg(table + pj);
+  if (page < 0 || page >= p.num_pages) {
+    set_err(p.err, DCP_ERRBIT_PAGE_RANGE);
+    return nullptr;
+  }
+  constexpr int tb = KVT == DCP_KV_BF16 ? kTokBytesBF16 : kTokBytesFP8;
+  return p.pool + ((int64_t)page * 64 + (l & 63)) * tb;
+}
+
+// Block-wide exclusive prefix of v (384 threads); returns the prefix, *total the sum.
+__device__ __forceinline__ int64_t block_scan_excl(int64_t v, TcShared& sh, int64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh.warp_sum[warp] = x;
+  __syncthreads();
+  int64_t base = 0, tot = 0;
+  for (int w = 0; w < kTcThreads / 32; ++w) {
+    if (w < warp) base += sh.warp_sum[w];
+    tot += sh.warp_sum[w];
+  }
+  __syncthreads();
+  *total = tot;
+  return base + x - v;
+}
+
+template <int KVT, bool FUSED, bool SPARSE>
+__global__ void __launch_bounds__(kTcThreads, 1)
+decode_tc_kernel(const DecodeParams p) {
+  using C = TcCfg<KVT>;
+  using L = TcLay<KVT>;
+  constexpr int TN = C::TN, NS = C::NS, NK = C::NK;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ TcShared sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_rank();
+  const uint32_t peer = crank ^ 1u;
+  const int pair = blockIdx.x >> 1;
+  const int P = p.pairs;
+  const int64_t U = p.num_units;
+  const int H = p.heads;
+  volatile int* abort_flag = &sh.abort_flag;
+
+  // ---------------------------------------------------------------- set-up
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&sh.stg_full[i], 1);
+      mbar_init(&sh.stg_empty[i], 128);
+    }
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&sh.kt_full[i], 128);
+      mbar_init(&sh.kt_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.p_full[i], 128);
+      mbar_init(&sh.in_full[i], 1);
+      mbar_init(&sh.out_free[i], 1);
+    }
+    mbar_init(&sh.pv_done, 1);
+    mbar_init(&sh.x_read[0], 128);
+    mbar_init(&sh.x_read[1], 128);
+    mbar_init(&sh.fin_pub, 128);
+    mbar_init(&sh.fin_dec, 1);
+    mbar_init(&sh.q_ready, 128);
+    mbar_init(&sh.drain, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+    // the exchange inboxes expect one tile of partial logits each
+    mbar_arrive_expect_tx(&sh.in_full[0], 128 * TN * 4);
+    mbar_arrive_expect_tx(&sh.in_full[1], 128 * TN * 4);
+  }
+
+  // this pair's contiguous range of the tile sequence
+  if (FUSED && SPARSE) {
+    const int64_t tu = (p.k + TN - 1) / TN;
+    const int64_t T = U * tu;
+    const int Pe = (int)(T < P ? (T > 0 ? T : 1) : P);
+    const int64_t t0 = pair < Pe ? pair * T / Pe : T, t1 = pair < Pe ? (pair + 1) * T / Pe : T;
+    if (tid == 0) {
+      sh.Peff = Pe;
+      sh.T = T;
+      sh.t0 = t0;
+      sh.ntiles = (int)(t1 - t0);
+      sh.unit0 = t0 < T ? t0 / tu : 0;
+      sh.tile0 = t0 < T ? (int)(t0 % tu) : 0;
+    }
+  } else {
+    int64_t part = 0;
+    for (int64_t u = tid; u < U; u += kTcThreads) part += get_unit<FUSED, SPARSE, TN>(p, u).ntile;
+    int64_t T;
+    block_scan_excl(part, sh, &T);
+    const int Pe = (int)(T < P ? (T > 0 ? T : 1) : P);
+    const int64_t t0 = pair < Pe ? pair * T / Pe : T, t1 = pair < Pe ? (pair + 1) * T / Pe : T;
+    if (tid == 0) {
+      sh.Peff = Pe;
+      sh.T = T;
+      sh.t0 = t0;
+      sh.ntiles = (int)(t1 - t0);
+      sh.unit0 = 0;
+      sh.tile0 = 0;
+      sh.scan_base = 0;
+    }
+    __syncthreads();
+    if (t1 > t0) {
+      for (int64_t c0 = 0; c0 < U; c0 += kTcThreads) {
+        const int64_t u = c0 + tid;
+        const int nt = u < U ? get_unit<FUSED, SPARSE, TN>(p, u).ntile : 0;
+        int64_t chunk_total;
+        const int64_t excl = block_scan_excl(nt, sh, &chunk_total) + sh.scan_base;
+        if (nt > 0 && t0 >= excl && t0 < excl + nt) {
+          sh.unit0 = u;
+          sh.tile0 = (int)(t0 - excl);
+        }
+        __syncthreads();
+        if (tid == 0) sh.scan_base += chunk_total;
+        __syncthreads();
+        if (sh.scan_base > t0) break;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // peers' barriers are initialised before any remote arrive / st.async
+  tc_fence_after();
+  const uint32_t tbase = sh.tmem_base;
+  const int ntiles = sh.ntiles;
+  const int64_t T = sh.T, t0 = sh.t0;
+
+  if (warp == 0) {
+    // ============================================================ producer
+    Walk<FUSED, SPARSE, TN> w;
+    w.init(p, sh.unit0, sh.tile0, ntiles);
+    int j = 0;
+    for (; j < ntiles; ++j) {
+      const int slot = j % NS;
+      if (!mbar_wait(&sh.stg_empty[slot], ((j / NS) & 1) ^ 1, abort_flag)) break;
+      const uint8_t* row = nullptr;
+      if (lane < TN) row = tc_resolve<KVT, FUSED, SPARSE>(p, w.info, w.u, w.lt * TN + lane);
+      const unsigned mask = __ballot_sync(0xffffffffu, row != nullptr);
+      unsigned char* stg = smem + L::OFF_STG + slot * L::STG_BYTES;
+      if (lane == 0) {
+        sh.stg_mask[slot] = mask;
+        mbar_arrive_expect_tx(&sh.stg_full[slot], __popc(mask) * L::STG_TOK);
+      }
+      __syncwarp();
+      if (row != nullptr) {
+        bulk_g2s(stg + lane * C::STG_LAT, row + crank * C::ROW_LAT, C::STG_LAT,
+                 &sh.stg_full[slot]);
+        bulk_g2s(stg + TN * C::STG_LAT + lane * 64, row + C::ROW_ROPE + crank * 64, 64,
+                 &sh.stg_full[slot]);
+        if (C::STG_SC)
+          bulk_g2s(stg + TN * (C::STG_LAT + 64) + lane * 16, row + C::ROW_SC, 16,
+                   &sh.stg_full[slot]);
+      }
+      w.next(p);
+    }
+    // never leave with copies in flight: wait for the last issued slots
+    for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) {
+      volatile int no_abort = 0;
+      mbar_wait(&sh.stg_full[jj % NS], (jj / NS) & 1, &no_abort);
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer
+    constexpr uint32_t idesc_qk = idesc_bf16(128, TN, 0, 0);
+    constexpr uint32_t idesc_pv = KVT == DCP_KV_BF16 ? idesc_bf16(128, 256, 0, 1)
+                                                     : idesc_bf16(128, 128, 0, 1);
+    const uint32_t qb = tbase + kColQ;
+    int q_phase = 0;
+    bool ok = true;
+    auto issue_qk = [&](int j, bool unit_first) -> bool {
+      if (unit_first) {
+        if (!mbar_wait(&sh.q_ready, q_phase & 1, abort_flag)) return false;
+        ++q_phase;
+      }
+      if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kt = smem_u32(smem + L::OFF_KT + (j % NK) * L::KT_BYTES);
+        const uint32_t sb = tbase + kColS + (j & 1) * L::SBUF;
+#pragma unroll
+        for (int ks = 0; ks < 18; ++ks) {
+          const uint64_t bd = smem_desc(kt + (ks >> 2) * L::BS + (ks & 3) * 32, 16, 1024);
+          if (KVT == DCP_KV_BF16) {
+            mma_ts(sb, qb + 8 * ks, bd, idesc_qk, ks > 0);
+          } else {
+            const int acc = ks < 8 ? 0 : ks < 16 ? 1 : 2;
+            const int k0 = acc * 8;
+            mma_ts(sb + acc * TN, qb + 8 * ks, bd, idesc_qk, ks > k0);
+          }
+        }
+        mma_commit(&sh.s_full[j & 1]);
+      }
+      __syncwarp();
+      return true;
+    };
+    Walk<FUSED, SPARSE, TN> w;
+    w.init(p, sh.unit0, sh.tile0, ntiles);
+    // the softmax warps load Q for the pair's first unit even when it starts mid-unit
+    if (ntiles > 0) ok = issue_qk(0, true);
+    for (int j = 0; ok && j < ntiles; ++j) {
+      if (j + 1 < ntiles) {
+        Walk<FUSED, SPARSE, TN> wn = w;
+        wn.next(p);
+        if (!(ok = issue_qk(j + 1, wn.first()))) break;
+      }
+      if (!(ok = mbar_wait(&sh.p_full[j & 1], (j >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kt = smem_u32(smem + L::OFF_KT + (j % NK) * L::KT_BYTES);
+        const uint32_t sb = tbase + kColS + (j & 1) * L::SBUF;
+        // a unit's (or this pair's) first tile overwrites O
+        const uint32_t acc0 = (w.first() || j == 0) ? 0u : 1u;
+        if (KVT == DCP_KV_BF16) {
+#pragma unroll
+          for (int kk = 0; kk < TN / 16; ++kk)
+            mma_ts(tbase + kColO, sb + 8 * kk, smem_desc(kt + kk * 2048, L::BS, 1024), idesc_pv,
+                   acc0 | (kk > 0));
+        } else {
+          mma_ts(tbase + kColO, sb, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
+          mma_ts(tbase + kColO + 128, sb + TN / 2, smem_desc(kt + 2 * L::BS, L::BS, 1024),
+                 idesc_pv, acc0);
+        }
+        mma_commit(&sh.kt_empty[j % NK]);
+        mma_commit(&sh.pv_done);
+      }
+      __syncwarp();
+      w.next(p);
+    }
+    if (lane == 0) mma_commit(&sh.drain);
+    __syncwarp();
+    volatile int no_abort = 0;
+    mbar_wait(&sh.drain, 0, &no_abort);  // no MMA in flight before TMEM is released
+  } else if (warp >= 4 && warp < 8) {
+    // ============================================================ converters
+    const int ct = tid - 128;
+    for (int j = 0; j < ntiles; ++j) {
+      const int slot = j % NS, ks = j % NK;
+      if (!mbar_wait(&sh.stg_full[slot], (j / NS) & 1, abort_flag)) break;
+      if (!mbar_wait(&sh.kt_empty[ks], ((j / NK) & 1) ^ 1, abort_flag)) break;
+      const uint32_t mask = sh.stg_mask[slot];
+      const unsigned char* stg = smem + L::OFF_STG + slot * L::STG_BYTES;
+      unsigned char* kt = smem + L::OFF_KT + ks * L::KT_BYTES;
+      unsigned char* meta = smem + L::OFF_META + ks * L::META_BYTES;
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      if (KVT == DCP_KV_FP8_E4M3_S128) {
+        for (int q = ct; q < TN * 16; q += 128) {  // 16 codes per chunk
+          const int t = q >> 4, ch = q & 15;
+          const uint4 v = (mask >> t) & 1
+                              ? *reinterpret_cast<const uint4*>(stg + t * 256 + ch * 16)
+                              : zero;
+          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o[2 * e] = e4m3x2_to_bf16x2_scaled((uint16_t)(in[e] & 0xffffu));
+            o[2 * e + 1] = e4m3x2_to_bf16x2_scaled((uint16_t)(in[e] >> 16));
+          }
+          unsigned char* base = kt + (ch >> 2) * L::BS + t * 128;
+          const int c16 = (ch & 3) * 2;
+          *reinterpret_cast<uint4*>(base + ((c16 ^ (t & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(base + (((c16 + 1) ^ (t & 7)) << 4)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (ct < TN * 4) {  // RoPE half: 32 bf16 = 4 chunks per slot
+          const int t = ct >> 2, c4 = ct & 3;
+          const uint4 v = (mask >> t) & 1
+                              ? *reinterpret_cast<const uint4*>(stg + TN * 256 + t * 64 + c4 * 16)
+                              : zero;
+          *reinterpret_cast<uint4*>(kt + 4 * L::BS + t * 128 + ((c4 ^ (t & 7)) << 4)) = v;
+        }
+        if (ct < TN) {  // this CTA's two block scales, premultiplied by 2^56
+          float2 sc = make_float2(0.f, 0.f);
+          if ((mask >> ct) & 1) {
+            const float4 s4 = *reinterpret_cast<const float4*>(stg + TN * (256 + 64) + ct * 16);
+            sc = crank == 0 ? make_float2(s4.x, s4.y) : make_float2(s4.z, s4.w);
+          }
+          reinterpret_cast<float2*>(meta + 16)[ct] = make_float2(sc.x * kTwo56, sc.y * kTwo56);
+        }
+      } else {
+        for (int q = ct; q < TN * 32; q += 128) {  // 8 bf16 per chunk
+          const int t = q >> 5, ch = q & 31;
+          const uint4 v = (mask >> t) & 1
+                              ? *reinterpret_cast<const uint4*>(stg + t * 512 + ch * 16)
+                              : zero;
+          *reinterpret_cast<uint4*>(kt + (ch >> 3) * L::BS + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = v;
+        }
+        {
+          const int t = ct >> 2, c4 = ct & 3;
+          const uint4 v = (mask >> t) & 1
+                              ? *reinterpret_cast<const uint4*>(stg + TN * 512 + t * 64 + c4 * 16)
+                              : zero;
+          *reinterpret_cast<uint4*>(kt + 4 * L::BS + t * 128 + ((c4 ^ (t & 7)) << 4)) = v;
+        }
+      }
+      if (ct == 0) *reinterpret_cast<uint32_t*>(meta) = mask;
+      fence_proxy_async_smem();
+      mbar_arrive(&sh.kt_full[ks]);
+      mbar_arrive(&sh.stg_empty[slot]);
+    }
+  } else if (warp >= 8) {
+    // ============================================================ softmax / epilogue
+    const int h = tid - 256;  // head = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t trow = tbase + lane_off;
+    const float sl2 = p.scale_log2;
+    float* xin = reinterpret_cast<float*>(smem + L::OFF_X);
+
+    // units without any slot: zero output, -inf LSE
+    if (!(FUSED && SPARSE)) {
+      for (int64_t u = pair; u < U; u += P) {
+        const UnitInfo x = get_unit<FUSED, SPARSE, TN>(p, u);
+        if (x.ntile != 0 || h >= H) continue;
+        const int64_t oi = (u * H + h) * kDv + crank * 256;
+        if (FUSED) {
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi);
+          for (int i = 0; i < 32; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi);
+          for (int i = 0; i < 64; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (crank == 0) p.lse[u * H + h] = -INFINITY;
+      }
+    }
+
+    auto load_q = [&](int64_t r) {
+      uint32_t w[16];
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(p.q) + (r * H + h) * kDqk);
+      for (int c = 0; c < 9; ++c) {  // 8 chunks of latent (4 x uint4 each) + 1 of RoPE
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (h < H) v = __ldg(src + (c < 8 ? crank * 32 + c * 4 + i : 64 + crank * 4 + i));
+          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+        tmem_st16(trow + kColQ + 16 * c, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sh.q_ready);
+    };
+
+    Walk<FUSED, SPARSE, TN> w;
+    w.init(p, sh.unit0, sh.tile0, ntiles);
+    if (ntiles > 0) load_q(w.info.r);
+    float m_ref = -INFINITY, lsum = 0.f;
+    int64_t U0 = t0 - sh.tile0;   // global index of the current unit's first tile
+    bool from_start = sh.tile0 == 0;
+    int slot_idx = 0;             // workspace slot of a split unit: 0 first unit, 1 last
+    int fin_phase = 0;
+    bool ok = true;
+
+    // Finish the current unit: normalise and write O (or a split partial) and the LSE.
+    auto finish_unit = [&](int jl, bool complete) {
+      volatile int no_abort = 0;
+      mbar_wait(&sh.pv_done, jl & 1, ok ? abort_flag : &no_abort);
+      tc_fence_after();
+      const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
+      const float fix = (KVT == DCP_KV_BF16 ? 1.0f : kTwo56) * inv;
+      const float lse_v = lsum > 0.f ? (m_ref + __log2f(lsum)) * kLn2 : -INFINITY;
+      const int64_t u = w.u;
+      const int64_t oi = (u * H + h) * kDv + crank * 256;
+      float* wso = p.tc_o + (((int64_t)pair * 2 + slot_idx) * 128 + h) * kDv + crank * 256;
+      for (int c = 0; c < 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(trow + kColO + 16 * c, v);
+        tmem_ld_wait();
+        float f[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]) * fix;
+        if (!complete) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            __stcg(reinterpret_cast<float4*>(wso + 16 * c) + i,
+                   make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]));
+        } else if (h < H) {
+          if (FUSED) {
+            uint32_t b2[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              __nv_bfloat162 t2 = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+              b2[i] = *reinterpret_cast<uint32_t*>(&t2);
+            }
+            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
+            o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
+            o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
+          } else {
+            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi + 16 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      if (complete) {
+        if (crank == 0 && h < H) p.lse[u * H + h] = lse_v;
+        return;
+      }
+      // split unit: publish, and merge if this pair finishes it last
+      __stcg(p.tc_l + (((int64_t)pair * 2 + slot_idx) * 2 + crank) * 128 + h, lse_v);
+      __threadfence();
+      const int64_t U1 = U0 + w.info.ntile;
+      const int64_t Pe = sh.Peff;  // pair q starts at tile q*T/Pe
+      const int64_t pf = min(Pe - 1, ((U0 + 1) * Pe - 1) / T);
+      const int64_t pl = min(Pe - 1, (U1 * Pe - 1) / T);
+      mbar_arrive(&sh.fin_pub);
+      if (warp == 8) {  // every thread of this CTA has published: take a ticket
+        if (lane == 0) {
+          sh.last_flag = 0;
+          if (mbar_wait(&sh.fin_pub, fin_phase & 1, abort_flag)) {
+            __threadfence();
+            const unsigned prev = atomicAdd(p.tc_cnt + u * 2 + crank, 1u);
+            sh.last_flag = prev == (unsigned)(pl - pf);
+          }
+          mbar_arrive(&sh.fin_dec);
+        }
+        __syncwarp();
+      }
+      const bool dec = mbar_wait(&sh.fin_dec, fin_phase & 1, abort_flag);
+      ++fin_phase;
+      if (!dec || !sh.last_flag) return;
+      __threadfence();
+      float mx = -INFINITY;
+      for (int64_t q = pf; q <= pl; ++q) {
+        const int sq = (q * T / Pe) >= U0 ? 0 : 1;
+        mx = fmaxf(mx, __ldcg(p.tc_l + ((q * 2 + sq) * 2 + crank) * 128 + h));
+      }
+      float W = 0.f;
+      float acc[16];
+      for (int c = 0; c < 16; ++c) {
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        W = 0.f;
+        if (mx != -INFINITY) {
+          for (int64_t q = pf; q <= pl; ++q) {
+            const int sq = (q * T / Pe) >= U0 ? 0 : 1;
+            const float lq = __ldcg(p.tc_l + ((q * 2 + sq) * 2 + crank) * 128 + h);
+            const float wq = fast_exp2((lq - mx) * kLog2e);
+            W += wq;
+            if (wq == 0.f) continue;
+            const float4* src = reinterpret_cast<const float4*>(
+                p.tc_o + ((q * 2 + sq) * 128 + h) * kDv + crank * 256 + 16 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 v4 = __ldcg(src + i);
+              acc[4 * i] = fmaf(wq, v4.x, acc[4 * i]);
+              acc[4 * i + 1] = fmaf(wq, v4.y, acc[4 * i + 1]);
+              acc[4 * i + 2] = fmaf(wq, v4.z, acc[4 * i + 2]);
+              acc[4 * i + 3] = fmaf(wq, v4.w, acc[4 * i + 3]);
+            }
+          }
+        }
+        const float iw = W > 0.f ? 1.0f / W : 0.f;
+        if (h < H) {
+          if (FUSED) {
+            uint32_t b2[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              __nv_bfloat162 t2 = __floats2bfloat162_rn(acc[2 * i] * iw, acc[2 * i + 1] * iw);
+              b2[i] = *reinterpret_cast<uint32_t*>(&t2);
+            }
+            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
+            o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
+            o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
+          } else {
+            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi + 16 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o[i] = make_float4(acc[4 * i] * iw, acc[4 * i + 1] * iw, acc[4 * i + 2] * iw,
+                                 acc[4 * i + 3] * iw);
+          }
+        }
+      }
+      if (crank == 0 && h < H) p.lse[u * H + h] = mx == -INFINITY ? -INFINITY : mx + __log2f(W) * kLn2;
+    };
+
+    int j = 0;
+    for (; j < ntiles; ++j) {
+      const int buf = j & 1;
+      if (!(ok = mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag))) break;
+      if (!(ok = mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag))) break;
+      tc_fence_after();
+      const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
+      const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
+      const float2* scl = reinterpret_cast<const float2*>(meta + 16);
+      const uint32_t sb = trow + kColS + buf * L::SBUF;
+      float s[TN];
+      {
+        uint32_t a[TN];
+        if (TN == 32) {
+          tmem_ld16(sb, a);
+          tmem_ld16(sb + 16, a + 16);
+        } else {
+          tmem_ld16(sb, a);
+        }
+        if (KVT == DCP_KV_BF16) {
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * sl2;
+        } else {
+          uint32_t b[TN], r[TN];
+          tmem_ld16(sb + TN, b);
+          tmem_ld16(sb + 2 * TN, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < TN; ++t) {
+            const float2 sc = scl[t];
+            const float x = fmaf(__uint_as_float(a[t]) * kTwo56, sc.x,
+                                 fmaf(__uint_as_float(b[t]) * kTwo56, sc.y, __uint_as_float(r[t])));
+            s[t] = x * sl2;
+          }
+        }
+      }
+      // next unit's queries go into TMEM once this tile's Q.K^T is done
+      if (w.last() && j + 1 < ntiles) {
+        Walk<FUSED, SPARSE, TN> wn = w;
+        wn.next(p);
+        load_q(wn.info.r);
+      }
+      // exchange partial logits with the peer CTA
+      const int x = j & 1;
+      if (!(ok = mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true))) break;
+      float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
+#pragma unroll
+      for (int c = 0; c < TN / 4; ++c)
+        st_async_v4(xrow + 4 * c, peer, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
+                    __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]), &sh.in_full[x]);
+      if (!(ok = mbar_wait(&sh.in_full[x], (j >> 1) & 1, abort_flag, true))) break;
+#pragma unroll
+      for (int c = 0; c < TN / 4; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * c);
+        s[4 * c] += v.x;
+        s[4 * c + 1] += v.y;
+        s[4 * c + 2] += v.z;
+        s[4 * c + 3] += v.w;
+      }
+      mbar_arrive(&sh.x_read[x]);
+      if (warp == 8) {  // once every thread has read it, inbox x may take the peer's next tile
+        int okx = 1;
+        if (lane == 0) {
+          okx = mbar_wait(&sh.x_read[x], (j >> 1) & 1, abort_flag);
+          if (okx) {
+            mbar_arrive_expect_tx(&sh.in_full[x], 128 * TN * 4);
+            mbar_arrive_cluster(&sh.out_free[x], peer);
+          }
+        }
+        okx = __shfl_sync(0xffffffffu, okx, 0);
+        if (!(ok = okx != 0)) break;
+      }
+      // online softmax (base 2) with a lazily raised reference
+      float mt = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < TN; ++t) {
+        if (!((mask >> t) & 1)) s[t] = -INFINITY;
+        mt = fmaxf(mt, s[t]);
+      }
+      // per head: raise the reference when the tile max exceeds it by more than 2^8; the
+      // TMEM read-modify-write of O is warp-collective, so a warp rescales when any of its
+      // heads needs it (alpha = 1 for the others)
+      float alpha = 1.0f;
+      const bool raise = mt > m_ref + 8.0f;
+      if (raise && m_ref != -INFINITY) alpha = fast_exp2(m_ref - mt);
+      if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+        if (!(ok = mbar_wait(&sh.pv_done, (j - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        for (int c = 0; c < 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(trow + kColO + 16 * c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st16(trow + kColO + 16 * c, v);
+        }
+      }
+      if (raise) {
+        lsum *= alpha;
+        m_ref = mt;
+      }
+      float pr[TN];
+#pragma unroll
+      for (int t = 0; t < TN; ++t) {
+        pr[t] = m_ref == -INFINITY ? 0.f : fast_exp2(s[t] - m_ref);
+        lsum += pr[t];
+      }
+      if (KVT == DCP_KV_BF16) {
+        uint32_t pw[TN / 2];
+#pragma unroll
+        for (int i = 0; i < TN / 2; ++i) {
+          __nv_bfloat162 t2 = __floats2bfloat162_rn(pr[2 * i], pr[2 * i + 1]);
+          pw[i] = *reinterpret_cast<uint32_t*>(&t2);
+        }
+        tmem_st16(sb, pw);
+      } else {
+        uint32_t plo[TN / 2], phi[TN / 2];
+#pragma unroll
+        for (int i = 0; i < TN / 2; ++i) {
+          const float2 s0 = scl[2 * i], s1 = scl[2 * i + 1];
+          __nv_bfloat162 a2 = __floats2bfloat162_rn(pr[2 * i] * s0.x, pr[2 * i + 1] * s1.x);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(pr[2 * i] * s0.y, pr[2 * i + 1] * s1.y);
+          plo[i] = *reinterpret_cast<uint32_t*>(&a2);
+          phi[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        tmem_st8(sb, plo);
+        tmem_st8(sb + TN / 2, phi);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sh.p_full[buf]);
+      if (w.last()) {
+        finish_unit(j, from_start);
+        m_ref = -INFINITY;
+        lsum = 0.f;
+        from_start = true;
+        slot_idx = 1;
+        U0 = t0 + j + 1;
+      }
+      w.next(p);
+    }
+    // the range ended inside a unit (Walk.next does not move past the last tile):
+    // publish that unit's partial
+    if (ok && j == ntiles && ntiles > 0 && w.lt != w.info.ntile - 1) finish_unit(ntiles - 1, false);
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+  if (tid == 0 && sh.abort_flag && p.err_timeout) atomicOr(p.err_timeout, DCP_ERRBIT_TIMEOUT);
+  cluster_sync();
+}
+
+// ------------------------------------------------------------------ host side
+static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t tc_workspace_bytes(int64_t units, int pairs) {
+  return a256((size_t)pairs * 2 * 128 * kDv * sizeof(float)) +
+         a256((size_t)pairs * 2 * 2 * 128 * sizeof(float)) +
+         a256((size_t)units * 2 * sizeof(unsigned));
+}
+
+void tc_bind_workspace(DecodeParams& p, void* ws) {
+  char* b = static_cast<char*>(ws);
+  const size_t o = a256((size_t)p.pairs * 2 * 128 * kDv * sizeof(float));
+  const size_t l = a256((size_t)p.pairs * 2 * 2 * 128 * sizeof(float));
+  p.tc_o = reinterpret_cast<float*>(b);
+  p.tc_l = reinterpret_cast<float*>(b + o);
+  p.tc_cnt = reinterpret_cast<unsigned*>(b + o + l);
+}
+
+size_t tc_ticket_bytes(int64_t units) { return (size_t)units * 2 * sizeof(unsigned); }
+
+int tc_pairs_for(int64_t units, int64_t tiles_bound) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+  }
+  int64_t pairs = sms / 2;
+  if (tiles_bound < pairs) pairs = tiles_bound > 0 ? tiles_bound : 1;
+  (void)units;
+  return (int)pairs;
+}
+
+int tc_tile_slots(int kv_dtype) { return kv_dtype == DCP_KV_BF16 ? 32 : 16; }
+
+// DCPMLA_PATH=simt selects the CUDA-core path for every head count (read at each call).
+bool tc_path_enabled() {
+  const char* e = getenv("DCPMLA_PATH");
+  return !(e && e[0] == 's');
+}
+
+template <int KVT, bool FUSED, bool SPARSE>
+static cudaError_t tc_launch_one(const DecodeParams& p, cudaStream_t st) {
+  auto kern = decode_tc_kernel<KVT, FUSED, SPARSE>;
+  const int smem = TcLay<KVT>::SMEM;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.pairs, 1, 1);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,
+                             cudaStream_t st) {
+  if (kv_dtype == DCP_KV_BF16) {
+    if (fused) return sparse ? tc_launch_one<DCP_KV_BF16, true, true>(p, st)
+                             : tc_launch_one<DCP_KV_BF16, true, false>(p, st);
+    return sparse ? tc_launch_one<DCP_KV_BF16, false, true>(p, st)
+                  : tc_launch_one<DCP_KV_BF16, false, false>(p, st);
+  }
+  if (fused) return sparse ? tc_launch_one<DCP_KV_FP8_E4M3_S128, true, true>(p, st)
+                           : tc_launch_one<DCP_KV_FP8_E4M3_S128, true, false>(p, st);
+  return sparse ? tc_launch_one<DCP_KV_FP8_E4M3_S128, false, true>(p, st)
+                : tc_launch_one<DCP_KV_FP8_E4M3_S128, false, false>(p, st);
+}
+
+}  // namespace dcp

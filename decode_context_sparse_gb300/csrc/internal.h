@@ -35,6 +35,13 @@ struct DecodeParams {
   float* ws_lse;          // [units][splits][H]
   unsigned* ws_cnt;       // tickets [units][head groups]
   int32_t* err;           // optional error word
+  // tensor-core path
+  int use_tc;             // 1: decode_tc_kernel, 0: decode_simt_kernel
+  int pairs;              // CTA pairs of the persistent grid
+  float* tc_o;            // split-unit partials [pairs][2][128][512]
+  float* tc_l;            // their LSEs [pairs][2][2][128]
+  unsigned* tc_cnt;       // tickets [units][2]
+  int32_t* err_timeout;   // error word for bounded-wait timeouts (whenever given)
 };
 
 cudaError_t launch_remap_topk(const int32_t* gidx, int64_t rows, int k, int D, int I, int shard,
@@ -51,6 +58,16 @@ int simt_auto_splits(int64_t units, int heads, int64_t max_tokens);
 void simt_bind_workspace(DecodeParams& p, void* ws);
 cudaError_t launch_decode_simt(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,
                                cudaStream_t st);
+
+// Tensor-core decode (48..128 heads, page size 64).
+size_t tc_workspace_bytes(int64_t units, int pairs);
+size_t tc_ticket_bytes(int64_t units);
+void tc_bind_workspace(DecodeParams& p, void* ws);
+int tc_pairs_for(int64_t units, int64_t tiles_bound);
+int tc_tile_slots(int kv_dtype);
+bool tc_path_enabled();
+cudaError_t launch_decode_tc(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,
+                             cudaStream_t st);
 
 // Host-side checks shared by the decode entry points; fills p (workspace not bound).
 int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t dcp,

@@ -58,6 +58,8 @@ typedef enum {
 /* Bits a kernel ORs into *err_flag (only when err_flag != NULL and checked != 0). */
 #define DCP_ERRBIT_SLOT_RANGE 1   /* a slot id past the block table row, or negative local id */
 #define DCP_ERRBIT_PAGE_RANGE 2   /* a block-table entry outside [0, num_pages) */
+#define DCP_ERRBIT_TIMEOUT 4      /* a kernel-internal wait gave up (reported whenever
+                                     err_flag != NULL); the outputs are then invalid */
 
 #define DCP_MAX_SHARDS 64
 #define DCP_MAX_TOPK 16384
