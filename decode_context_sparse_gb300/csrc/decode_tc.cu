@@ -90,8 +90,7 @@ struct TcLay {
 
 struct TcShared {
   uint64_t stg_full[4], stg_empty[4], kt_full[3], kt_empty[3];
-  uint64_t s_full[2], p_full[2], pv_done, q_ready, in_full[2], out_free[2], drain;
-  uint64_t x_read[2];         // all softmax threads have read inbox x
+  uint64_t s_full[2], p_full[2], pv_done[2], q_ready, in_full[2], out_free[2], drain;
   uint64_t fin_pub, fin_dec;  // split-unit publish / merge decision
   uint32_t stg_mask[4];
   uint32_t tmem_base;
@@ -228,31 +227,30 @@ decode_tc_kernel(const DecodeParams p) {
   volatile int* abort_flag = &sh.abort_flag;
 
   // ---------------------------------------------------------------- set-up
-  if (warp == 1) {
+  if (warp == 0) {
     tmem_alloc(&sh.tmem_base, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sh.stg_full[i], 1);
-      mbar_init(&sh.stg_empty[i], 128);
+      mbar_init(&sh.stg_full[i], 33);  // 32 copy-completion arrivals + 1 mask publication
+      mbar_init(&sh.stg_empty[i], 4);
     }
     for (int i = 0; i < NK; ++i) {
-      mbar_init(&sh.kt_full[i], 128);
+      mbar_init(&sh.kt_full[i], 4);
       mbar_init(&sh.kt_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.p_full[i], 128);
+      mbar_init(&sh.p_full[i], 4);
       mbar_init(&sh.in_full[i], 1);
-      mbar_init(&sh.out_free[i], 1);
+      mbar_init(&sh.out_free[i], 4);  // one arrival per softmax warp of the peer
     }
-    mbar_init(&sh.pv_done, 1);
-    mbar_init(&sh.x_read[0], 128);
-    mbar_init(&sh.x_read[1], 128);
-    mbar_init(&sh.fin_pub, 128);
+    mbar_init(&sh.pv_done[0], 1);
+    mbar_init(&sh.pv_done[1], 1);
+    mbar_init(&sh.fin_pub, 4);
     mbar_init(&sh.fin_dec, 1);
-    mbar_init(&sh.q_ready, 128);
+    mbar_init(&sh.q_ready, 4);
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -317,45 +315,121 @@ decode_tc_kernel(const DecodeParams p) {
   const int ntiles = sh.ntiles;
   const int64_t T = sh.T, t0 = sh.t0;
 
-  if (warp == 0) {
-    // ============================================================ producer
-    Walk<FUSED, SPARSE, TN> w;
-    w.init(p, sh.unit0, sh.tile0, ntiles);
-    int j = 0;
-    for (; j < ntiles; ++j) {
-      const int slot = j % NS;
-      if (!mbar_wait(&sh.stg_empty[slot], ((j / NS) & 1) ^ 1, abort_flag)) break;
-      const uint8_t* row = nullptr;
-      if (lane < TN) row = tc_resolve<KVT, FUSED, SPARSE>(p, w.info, w.u, w.lt * TN + lane);
-      const unsigned mask = __ballot_sync(0xffffffffu, row != nullptr);
-      unsigned char* stg = smem + L::OFF_STG + slot * L::STG_BYTES;
-      if (lane == 0) {
-        sh.stg_mask[slot] = mask;
-        mbar_arrive_expect_tx(&sh.stg_full[slot], __popc(mask) * L::STG_TOK);
+  if (warp >= 1 && warp <= 3) {
+    // ============================================================ loaders
+    // Warp 1+li takes tiles j = li, li+3, ...  A three-stage software pipeline hides the
+    // dependent loads: stage I loads the tile's slot ids (two tiles of this warp ahead),
+    // stage T maps them to owner shard / local slot and loads the block-table entry (one
+    // tile ahead), stage C turns pages into row addresses and issues 16-B cp.async copies
+    // of this CTA's share of each row into the staging slot.
+    constexpr int NLD = 3;
+    constexpr int CH_LAT = C::STG_LAT / 16, CH = CH_LAT + 4 + C::STG_SC / 16;
+    constexpr int tb = KVT == DCP_KV_BF16 ? kTokBytesBF16 : kTokBytesFP8;
+    const int li = warp - 1;
+    Walk<FUSED, SPARSE, TN> wi;
+    wi.init(p, sh.unit0, sh.tile0, ntiles);
+    for (int k = 0; k < li && k + 1 < ntiles; ++k) wi.next(p);
+    int t_v = -1;                   // stage T: slot id (global, local, or position)
+    bool t_has = false;             // stage T: the position holds a slot of the unit
+    UnitInfo t_x = wi.info;
+    int c_page = -1, c_l = -1;      // stage C: page and local slot (c_l < 0: no slot)
+    for (int n = 0;; ++n) {
+      const int jc = li + NLD * (n - 2), jt = jc + NLD, ji = jt + NLD;
+      if (jc >= ntiles) break;
+      if (jc >= 0) {
+        const int slot = jc % NS;
+        if (!mbar_wait(&sh.stg_empty[slot], ((jc / NS) & 1) ^ 1, abort_flag)) break;
+        const uint8_t* row = nullptr;
+        if (c_l >= 0) {
+          if (c_page >= 0 && c_page < p.num_pages)
+            row = p.pool + ((int64_t)c_page * 64 + (c_l & 63)) * tb;
+          else
+            set_err(p.err, DCP_ERRBIT_PAGE_RANGE);
+        }
+        const unsigned mask = __ballot_sync(0xffffffffu, row != nullptr);
+        unsigned char* stg = smem + L::OFF_STG + slot * L::STG_BYTES;
+        const unsigned long long rowv = reinterpret_cast<unsigned long long>(row);
+#pragma unroll 4
+        for (int it = 0; it < (TN * CH + 31) / 32; ++it) {
+          const int c = it * 32 + lane;
+          const int tok = min(c / CH, TN - 1), sub = c - tok * CH;
+          const uint8_t* r = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, rowv, tok));
+          if (c < TN * CH && r != nullptr) {
+            const uint8_t* src;
+            unsigned char* dst;
+            if (sub < CH_LAT) {
+              src = r + crank * C::ROW_LAT + sub * 16;
+              dst = stg + tok * C::STG_LAT + sub * 16;
+            } else if (sub < CH_LAT + 4) {
+              src = r + C::ROW_ROPE + crank * 64 + (sub - CH_LAT) * 16;
+              dst = stg + TN * C::STG_LAT + tok * 64 + (sub - CH_LAT) * 16;
+            } else {
+              src = r + C::ROW_SC;
+              dst = stg + TN * (C::STG_LAT + 64) + tok * 16;
+            }
+            cp_async16(dst, src);
+          }
+        }
+        if (lane == 0) sh.stg_mask[slot] = mask;
+        __syncwarp();
+        cp_async_arrive_noinc(&sh.stg_full[slot]);     // when this lane's copies land
+        if (lane == 0) mbar_arrive(&sh.stg_full[slot]);  // publishes the mask
       }
-      __syncwarp();
-      if (row != nullptr) {
-        bulk_g2s(stg + lane * C::STG_LAT, row + crank * C::ROW_LAT, C::STG_LAT,
-                 &sh.stg_full[slot]);
-        bulk_g2s(stg + TN * C::STG_LAT + lane * 64, row + C::ROW_ROPE + crank * 64, 64,
-                 &sh.stg_full[slot]);
-        if (C::STG_SC)
-          bulk_g2s(stg + TN * (C::STG_LAT + 64) + lane * 16, row + C::ROW_SC, 16,
-                   &sh.stg_full[slot]);
+      // stage T for tile jt
+      int n_page = -1, n_l = -1;
+      if (jt >= 0 && jt < ntiles && t_has && t_v < 0 && !FUSED)
+        set_err(p.err, DCP_ERRBIT_SLOT_RANGE);  // a negative local id among the valid ones
+      if (jt >= 0 && jt < ntiles && t_has && t_v >= 0) {
+        int l;
+        const int32_t* table;
+        if (FUSED) {
+          const int s = owner_of(t_v, p.D, p.I);
+          l = local_of(t_v, p.D, p.I);
+          table = p.bt + ((int64_t)s * p.num_seqs + t_x.b) * p.bt_stride;
+        } else {
+          l = t_v;
+          table = p.bt + ((int64_t)t_x.shard * p.num_seqs + t_x.b) * p.bt_stride;
+        }
+        const int pj = l >> 6;
+        if (pj < p.bt_stride) {
+          n_page = __ldg(table + pj);  // consumed in stage C, one tile of this warp later
+          n_l = l;
+        } else {
+          set_err(p.err, DCP_ERRBIT_SLOT_RANGE);
+        }
       }
-      w.next(p);
+      // stage I for tile ji
+      int n_v = -1;
+      bool n_has = false;
+      const UnitInfo n_x = wi.info;
+      if (ji < ntiles && lane < TN) {
+        const int pos = wi.lt * TN + lane;
+        if (pos < wi.info.n) {
+          n_has = true;
+          if (SPARSE) {
+            const int64_t base = FUSED ? wi.info.r * (int64_t)p.k : wi.u * (int64_t)p.k;
+            n_v = __ldg(p.idx + base + pos);  // consumed in stage T
+          } else {
+            n_v = pos;
+          }
+        }
+      }
+      if (ji < ntiles)
+        for (int k = 0; k < NLD; ++k) wi.next(p);
+      c_page = n_page;
+      c_l = n_l;
+      t_v = n_v;
+      t_has = n_has;
+      t_x = n_x;
     }
-    // never leave with copies in flight: wait for the last issued slots
-    for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) {
-      volatile int no_abort = 0;
-      mbar_wait(&sh.stg_full[jj % NS], (jj / NS) & 1, &no_abort);
-    }
-  } else if (warp == 1) {
+    cp_async_wait_all();  // no copy in flight when the CTA winds down
+  } else if (warp == 0) {
     // ============================================================ MMA issuer
     constexpr uint32_t idesc_qk = idesc_bf16(128, TN, 0, 0);
     constexpr uint32_t idesc_pv = KVT == DCP_KV_BF16 ? idesc_bf16(128, 256, 0, 1)
                                                      : idesc_bf16(128, 128, 0, 1);
     const uint32_t qb = tbase + kColQ;
+    const uint32_t leader = elect_one();
     int q_phase = 0;
     bool ok = true;
     auto issue_qk = [&](int j, bool unit_first) -> bool {
@@ -364,61 +438,78 @@ decode_tc_kernel(const DecodeParams p) {
         ++q_phase;
       }
       if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) return false;
+      // S buffer j&1 last held P(j-3) (P(m) is written into buffer (m+1)&1): its P.V must
+      // have read it -- the tensor pipe does not order that read before this write
+      if (j >= 3 && !mbar_wait(&sh.pv_done[(j - 3) & 1], ((j - 3) >> 1) & 1, abort_flag))
+        return false;
       tc_fence_after();
-      if (lane == 0) {
+      {  // issued by one elected lane of the converged warp (operands stay warp-uniform)
         const uint32_t kt = smem_u32(smem + L::OFF_KT + (j % NK) * L::KT_BYTES);
         const uint32_t sb = tbase + kColS + (j & 1) * L::SBUF;
+        const uint64_t kd = smem_desc(kt, 16, 1024);
 #pragma unroll
-        for (int ks = 0; ks < 18; ++ks) {
-          const uint64_t bd = smem_desc(kt + (ks >> 2) * L::BS + (ks & 3) * 32, 16, 1024);
+        for (int i = 0; i < 18; ++i) {
+          // FP8: the two latent-block chains are interleaved so that consecutive MMAs
+          // write different accumulators
+          const int ks = KVT == DCP_KV_BF16 ? i : (i < 16 ? (i >> 1) + 8 * (i & 1) : i);
+          // start-address field (bits 0-13, address >> 4) of a constant offset from kd
+          const uint64_t bd = kd + (uint64_t)((((ks >> 2) * L::BS + (ks & 3) * 32)) >> 4);
           if (KVT == DCP_KV_BF16) {
-            mma_ts(sb, qb + 8 * ks, bd, idesc_qk, ks > 0);
+            mma_ts_if(leader, sb, qb + 8 * ks, bd, idesc_qk, ks > 0);
           } else {
             const int acc = ks < 8 ? 0 : ks < 16 ? 1 : 2;
             const int k0 = acc * 8;
-            mma_ts(sb + acc * TN, qb + 8 * ks, bd, idesc_qk, ks > k0);
+            mma_ts_if(leader, sb + acc * TN, qb + 8 * ks, bd, idesc_qk, ks > k0);
           }
         }
-        mma_commit(&sh.s_full[j & 1]);
+        mma_commit_if(leader, &sh.s_full[j & 1]);
       }
-      __syncwarp();
       return true;
     };
-    Walk<FUSED, SPARSE, TN> w;
+    // Q.K^T runs two tiles ahead of P.V: QK(j+2) overwrites S buffer j&1, which needs
+    // A(j) to have read S(j) (implied by p_full(j-1)) and P.V(j-1) to have read P(j-1)
+    // (waited for in issue_qk); for j = 0 the first condition is only known after p_full(0).
+    Walk<FUSED, SPARSE, TN> w, wq;
     w.init(p, sh.unit0, sh.tile0, ntiles);
+    wq = w;
     // the softmax warps load Q for the pair's first unit even when it starts mid-unit
     if (ntiles > 0) ok = issue_qk(0, true);
+    if (ok && ntiles > 1) {
+      wq.next(p);
+      ok = issue_qk(1, wq.first());
+    }
     for (int j = 0; ok && j < ntiles; ++j) {
-      if (j + 1 < ntiles) {
-        Walk<FUSED, SPARSE, TN> wn = w;
-        wn.next(p);
-        if (!(ok = issue_qk(j + 1, wn.first()))) break;
+      if (j >= 1 && j + 2 < ntiles) {
+        wq.next(p);
+        if (!(ok = issue_qk(j + 2, wq.first()))) break;
       }
       if (!(ok = mbar_wait(&sh.p_full[j & 1], (j >> 1) & 1, abort_flag))) break;
       tc_fence_after();
-      if (lane == 0) {
+      {
         const uint32_t kt = smem_u32(smem + L::OFF_KT + (j % NK) * L::KT_BYTES);
-        const uint32_t sb = tbase + kColS + (j & 1) * L::SBUF;
+        const uint32_t sb = tbase + kColS + ((j + 1) & 1) * L::SBUF;  // P(j)
         // a unit's (or this pair's) first tile overwrites O
         const uint32_t acc0 = (w.first() || j == 0) ? 0u : 1u;
         if (KVT == DCP_KV_BF16) {
 #pragma unroll
           for (int kk = 0; kk < TN / 16; ++kk)
-            mma_ts(tbase + kColO, sb + 8 * kk, smem_desc(kt + kk * 2048, L::BS, 1024), idesc_pv,
-                   acc0 | (kk > 0));
+            mma_ts_if(leader, tbase + kColO, sb + 8 * kk, smem_desc(kt + kk * 2048, L::BS, 1024),
+                      idesc_pv, acc0 | (kk > 0));
         } else {
-          mma_ts(tbase + kColO, sb, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
-          mma_ts(tbase + kColO + 128, sb + TN / 2, smem_desc(kt + 2 * L::BS, L::BS, 1024),
-                 idesc_pv, acc0);
+          mma_ts_if(leader, tbase + kColO, sb, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
+          mma_ts_if(leader, tbase + kColO + 128, sb + TN / 2,
+                    smem_desc(kt + 2 * L::BS, L::BS, 1024), idesc_pv, acc0);
         }
-        mma_commit(&sh.kt_empty[j % NK]);
-        mma_commit(&sh.pv_done);
+        mma_commit_if(leader, &sh.kt_empty[j % NK]);
+        mma_commit_if(leader, &sh.pv_done[j & 1]);
       }
-      __syncwarp();
+      if (j == 0 && 2 < ntiles) {
+        wq.next(p);
+        if (!(ok = issue_qk(2, wq.first()))) break;
+      }
       w.next(p);
     }
-    if (lane == 0) mma_commit(&sh.drain);
-    __syncwarp();
+    mma_commit_elect(&sh.drain);
     volatile int no_abort = 0;
     mbar_wait(&sh.drain, 0, &no_abort);  // no MMA in flight before TMEM is released
   } else if (warp >= 4 && warp < 8) {
@@ -485,8 +576,11 @@ decode_tc_kernel(const DecodeParams p) {
       }
       if (ct == 0) *reinterpret_cast<uint32_t*>(meta) = mask;
       fence_proxy_async_smem();
-      mbar_arrive(&sh.kt_full[ks]);
-      mbar_arrive(&sh.stg_empty[slot]);
+      __syncwarp();
+      if (lane == 0) {  // one arrival per warp (arrivals of 128 threads serialise)
+        mbar_arrive(&sh.kt_full[ks]);
+        mbar_arrive(&sh.stg_empty[slot]);
+      }
     }
   } else if (warp >= 8) {
     // ============================================================ softmax / epilogue
@@ -528,7 +622,8 @@ decode_tc_kernel(const DecodeParams p) {
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sh.q_ready);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.q_ready);
     };
 
     Walk<FUSED, SPARSE, TN> w;
@@ -544,7 +639,7 @@ decode_tc_kernel(const DecodeParams p) {
     // Finish the current unit: normalise and write O (or a split partial) and the LSE.
     auto finish_unit = [&](int jl, bool complete) {
       volatile int no_abort = 0;
-      mbar_wait(&sh.pv_done, jl & 1, ok ? abort_flag : &no_abort);
+      mbar_wait(&sh.pv_done[jl & 1], (jl >> 1) & 1, ok ? abort_flag : &no_abort);
       tc_fence_after();
       const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
       const float fix = (KVT == DCP_KV_BF16 ? 1.0f : kTwo56) * inv;
@@ -595,7 +690,8 @@ decode_tc_kernel(const DecodeParams p) {
       const int64_t Pe = sh.Peff;  // pair q starts at tile q*T/Pe
       const int64_t pf = min(Pe - 1, ((U0 + 1) * Pe - 1) / T);
       const int64_t pl = min(Pe - 1, (U1 * Pe - 1) / T);
-      mbar_arrive(&sh.fin_pub);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.fin_pub);
       if (warp == 8) {  // every thread of this CTA has published: take a ticket
         if (lane == 0) {
           sh.last_flag = 0;
@@ -665,58 +761,81 @@ decode_tc_kernel(const DecodeParams p) {
       if (crank == 0 && h < H) p.lse[u * H + h] = mx == -INFINITY ? -INFINITY : mx + __log2f(W) * kLn2;
     };
 
-    int j = 0;
-    for (; j < ntiles; ++j) {
+    // Stage A(j): read tile j's logits from TMEM, form this CTA's partial, send it to the
+    // peer.  Stage B(j): add the peer's partial, online softmax, P into TMEM, finish the
+    // unit.  Order A(0), A(1), B(0), A(2), B(1), ...: tile j's exchange is in flight while
+    // A(j+1) runs, so the DSMEM round trip leaves the critical path.
+    auto stage_a = [&](int j, const Walk<FUSED, SPARSE, TN>& wa, float (&s)[TN]) -> bool {
       const int buf = j & 1;
-      if (!(ok = mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag))) break;
-      if (!(ok = mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag))) break;
+      if (!mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag)) return false;
+      if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) return false;
       tc_fence_after();
       const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
-      const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
       const float2* scl = reinterpret_cast<const float2*>(meta + 16);
       const uint32_t sb = trow + kColS + buf * L::SBUF;
-      float s[TN];
-      {
-        uint32_t a[TN];
-        if (TN == 32) {
-          tmem_ld16(sb, a);
-          tmem_ld16(sb + 16, a + 16);
-        } else {
-          tmem_ld16(sb, a);
-        }
-        if (KVT == DCP_KV_BF16) {
-          tmem_ld_wait();
+      uint32_t a[TN];
+      if (TN == 32) {
+        tmem_ld16(sb, a);
+        tmem_ld16(sb + 16, a + 16);
+      } else {
+        tmem_ld16(sb, a);
+      }
+      if (KVT == DCP_KV_BF16) {
+        tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * sl2;
-        } else {
-          uint32_t b[TN], r[TN];
-          tmem_ld16(sb + TN, b);
-          tmem_ld16(sb + 2 * TN, r);
-          tmem_ld_wait();
+        for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * sl2;
+      } else {
+        uint32_t b[TN], r[TN];
+        tmem_ld16(sb + TN, b);
+        tmem_ld16(sb + 2 * TN, r);
+        tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < TN; ++t) {
-            const float2 sc = scl[t];
-            const float x = fmaf(__uint_as_float(a[t]) * kTwo56, sc.x,
-                                 fmaf(__uint_as_float(b[t]) * kTwo56, sc.y, __uint_as_float(r[t])));
-            s[t] = x * sl2;
-          }
+        for (int t = 0; t < TN; ++t) {
+          const float2 sc = scl[t];
+          const float x = fmaf(__uint_as_float(a[t]) * kTwo56, sc.x,
+                               fmaf(__uint_as_float(b[t]) * kTwo56, sc.y, __uint_as_float(r[t])));
+          s[t] = x * sl2;
         }
       }
-      // next unit's queries go into TMEM once this tile's Q.K^T is done
-      if (w.last() && j + 1 < ntiles) {
-        Walk<FUSED, SPARSE, TN> wn = w;
+      // the next unit's queries go into TMEM once this tile's Q.K^T is done
+      if (wa.last() && j + 1 < ntiles) {
+        Walk<FUSED, SPARSE, TN> wn = wa;
         wn.next(p);
         load_q(wn.info.r);
       }
-      // exchange partial logits with the peer CTA
       const int x = j & 1;
-      if (!(ok = mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true))) break;
+      if (!mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true)) return false;
       float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c)
         st_async_v4(xrow + 4 * c, peer, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
                     __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]), &sh.in_full[x]);
+      return true;
+    };
+
+    float s_cur[TN], s_nxt[TN];
+    int j = 0;
+    if (ntiles > 0) ok = stage_a(0, w, s_cur);
+    for (; ok && j < ntiles; ++j) {
+      if (j + 1 < ntiles) {
+        Walk<FUSED, SPARSE, TN> wn = w;
+        wn.next(p);
+        if (!(ok = stage_a(j + 1, wn, s_nxt))) break;
+      }
+      // ---- stage B(j)
+      const int buf = j & 1;
+      const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
+      const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
+      const float2* scl = reinterpret_cast<const float2*>(meta + 16);
+      // P(j) goes into S buffer (j+1)&1: A(j+1) has already read S(j+1) out of it, and
+      // P(j-2), which it held before, has been read by P.V(j-2) (waited for below)
+      const uint32_t sb = trow + kColS + ((j + 1) & 1) * L::SBUF;
+      float s[TN];
+#pragma unroll
+      for (int t = 0; t < TN; ++t) s[t] = s_cur[t];
+      const int x = j & 1;
       if (!(ok = mbar_wait(&sh.in_full[x], (j >> 1) & 1, abort_flag, true))) break;
+      const float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c) {
         const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * c);
@@ -725,19 +844,9 @@ decode_tc_kernel(const DecodeParams p) {
         s[4 * c + 2] += v.z;
         s[4 * c + 3] += v.w;
       }
-      mbar_arrive(&sh.x_read[x]);
-      if (warp == 8) {  // once every thread has read it, inbox x may take the peer's next tile
-        int okx = 1;
-        if (lane == 0) {
-          okx = mbar_wait(&sh.x_read[x], (j >> 1) & 1, abort_flag);
-          if (okx) {
-            mbar_arrive_expect_tx(&sh.in_full[x], 128 * TN * 4);
-            mbar_arrive_cluster(&sh.out_free[x], peer);
-          }
-        }
-        okx = __shfl_sync(0xffffffffu, okx, 0);
-        if (!(ok = okx != 0)) break;
-      }
+      // inbox x is re-armed for the peer's next tile now (its phase is complete); each warp
+      // hands its rows back to the peer at the end of this stage
+      if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&sh.in_full[x], 128 * TN * 4);
       // online softmax (base 2) with a lazily raised reference
       float mt = -INFINITY;
 #pragma unroll
@@ -752,7 +861,7 @@ decode_tc_kernel(const DecodeParams p) {
       const bool raise = mt > m_ref + 8.0f;
       if (raise && m_ref != -INFINITY) alpha = fast_exp2(m_ref - mt);
       if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-        if (!(ok = mbar_wait(&sh.pv_done, (j - 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait(&sh.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         for (int c = 0; c < 16; ++c) {
           uint32_t v[16];
@@ -773,6 +882,8 @@ decode_tc_kernel(const DecodeParams p) {
         pr[t] = m_ref == -INFINITY ? 0.f : fast_exp2(s[t] - m_ref);
         lsum += pr[t];
       }
+      if (j >= 2 && !(ok = mbar_wait(&sh.pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
       if (KVT == DCP_KV_BF16) {
         uint32_t pw[TN / 2];
 #pragma unroll
@@ -796,7 +907,12 @@ decode_tc_kernel(const DecodeParams p) {
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sh.p_full[buf]);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh.p_full[buf]);
+        // this warp's inbox rows were read (and used) above: a relaxed arrive suffices
+        mbar_arrive_cluster_relaxed(&sh.out_free[x], peer);
+      }
       if (w.last()) {
         finish_unit(j, from_start);
         m_ref = -INFINITY;
@@ -805,6 +921,8 @@ decode_tc_kernel(const DecodeParams p) {
         slot_idx = 1;
         U0 = t0 + j + 1;
       }
+#pragma unroll
+      for (int t = 0; t < TN; ++t) s_cur[t] = s_nxt[t];
       w.next(p);
     }
     // the range ended inside a unit (Walk.next does not move past the last tile):
@@ -815,7 +933,7 @@ decode_tc_kernel(const DecodeParams p) {
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
