@@ -104,4 +104,7 @@ def test_decode_rejects_bad_arguments(lib):
     assert fused(R(_args(num_splits=4)), 8, 1, None) == dcp.DCP_ERR_WORKSPACE
     assert lib.mla_decode_workspace_size(R(_args(num_splits=4)), 8, 1) > 0
     assert lib.mla_decode_workspace_size(R(_args(q=None)), 8, 1) == ctypes.c_size_t(-1).value
-    assert lib.mla_decode_workspace_size(R(_args(num_splits=1)), 8, 1) == 0
+    # the CUDA-core path (up to 32 heads) needs none without splits; the tensor-core path
+    # (48..128 heads) always reserves its split-unit partials and tickets
+    assert lib.mla_decode_workspace_size(R(_args(num_splits=1, heads=32)), 8, 1) == 0
+    assert lib.mla_decode_workspace_size(R(_args(num_splits=1)), 8, 1) > 0
