@@ -78,7 +78,8 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   p.ws_cnt = nullptr;
   p.err = a->checked ? a->err_flag : nullptr;
   // tensor-core path for 48..128 heads (rows of up to 128 heads, padded)
-  p.use_tc = (tc_path_enabled() && a->heads > 32) ? 1 : 0;
+  // (the tensor-core path addresses pool rows with 32-bit gather coordinates)
+  p.use_tc = (tc_path_enabled() && a->heads > 32 && a->num_pages <= (int64_t)(INT32_MAX / 64)) ? 1 : 0;
   p.pairs = 0;
   p.tc_o = p.tc_l = nullptr;
   p.tc_cnt = nullptr;

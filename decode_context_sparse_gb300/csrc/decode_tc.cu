@@ -10,37 +10,43 @@
 // each row: CTA c owns latent dims [256c, 256c+256) and RoPE dims [512+32c, 512+32c+32)
 // of every key, computes the partial logits q.k over its 288 dims and the output columns
 // of its 256 value dims.  The two partial logit tiles are exchanged through distributed
-// shared memory (st.async counted on the peer's mbarrier), both CTAs run the same
-// softmax, and neither ever loads a KV byte the other loads.
+// shared memory (st.async counted on the peer's mbarrier) and both CTAs run the same
+// softmax.
 //
-// Per CTA (384 threads):
-//   warp 0      producer: resolves slot -> owner shard -> page and bulk-copies this CTA's
-//               share of each KV row (latent half, RoPE half, FP8 scales) into a staging
-//               ring (cp.async.bulk, completion counted in bytes);
-//   warp 1      TMEM owner and MMA issuer (one thread): S = Q K^T with Q as the A operand
-//               in TMEM, then O += P V with P as the A operand in TMEM;
-//   warps 4-7   converters: staging -> SWIZZLE_128B bf16 K tile (FP8: E4M3 -> bf16 times
-//               2^-112, exact), zero rows for padding, tile metadata (mask, scales);
+// Per CTA (384 threads), tiles of 32 key slots:
+//   warps 1-3   loaders (tiles round-robin): slot id -> owner shard / local slot -> page
+//               (a three-stage software pipeline over the dependent loads), then 4-row TMA
+//               gathers of this CTA's latent half and of the row tail into a staging ring;
+//   warp 0      TMEM owner and MMA issuer: S = Q K^T (latent part of Q in TMEM, RoPE part
+//               of Q in shared memory), then O += P V with P as the A operand in TMEM;
+//   warps 4-7   converters: staging -> SWIZZLE_128B bf16 K tile (FP8: E4M3 -> bf16,
+//               exact), zero rows for padding, per-slot scales;
 //   warps 8-11  softmax: thread h owns head h (TMEM lane h): reads its logits, exchanges
 //               partial logits with the peer, online softmax in base 2 with a lazily
 //               raised reference max (the output is rescaled only when the max grows by
 //               more than 2^8), writes P as bf16 into TMEM, and at the end of a row
 //               normalises O and writes it out (or merges split rows).
-// TMEM columns: O [0,256) | Q [256,400) | two logit buffers from 400 (FP8: three
-// accumulators per buffer -- latent block lo, latent block hi, RoPE -- since the FP8
-// scales differ per 128-block; BF16: one); P overwrites its logit buffer after the read.
+// TMEM columns: O [0,256) | Q latent [256,384) | two logit buffers from 384; P overwrites
+// the other logit buffer once that buffer's logits have been read.
 //
-// FP8 numerics: the latent lives in shared memory as exact bf16 images of e4m3 * 2^-112;
-// each 128-block's partial logit is scaled in fp32 by (scale * 2^56) * 2^56, so the
-// logits carry fp32 accuracy; for P V the block scale is folded into P (P * scale * 2^56
-// in bf16) and O is multiplied by 2^56 at the end.
+// FP8 numerics.  Each CTA's 256 latent dims are two 128-blocks with their own scales
+// s_lo, s_hi, so the logit needs two accumulators: acc_lo = q_lo . k_lo and
+// acc_hi = q_hi . k_hi over the exact E4M3 values.  The RoPE part rides in acc_lo: its
+// keys are stored as k_rope / s_lo split into a bf16 high part and a bf16 remainder
+// (about 16 significant bits), so that s_lo * acc_lo + s_hi * acc_hi is the logit with
+// fp32 accuracy.  (|s_lo| below 2^-60 is taken as 2^-60 for this purpose; the latent
+// term it then adds is below 2^-51 |q|.)  For P V the block scales are folded into P:
+// O[:, lo] += (P s_lo) V_lo, O[:, hi] += (P s_hi) V_hi.
 //
-// Work: a persistent grid of pairs; the concatenated sequence of 16/32-slot tiles of all
+// Work: a persistent grid of pairs; the concatenated sequence of 32-slot tiles of all
 // units (rows, or (shard, row) pairs) is cut into equal contiguous ranges, one per pair.
 // A unit cut by a range edge leaves fp32 partials in the workspace; the last pair to
 // finish it (atomic ticket, no waiting) merges them.  Every wait is bounded; a wait that
 // expires sets an abort flag, the CTA winds down and DCP_ERRBIT_TIMEOUT is reported.
+#include <cuda.h>
 #include <stdlib.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -49,43 +55,56 @@
 namespace dcp {
 using namespace tc;
 
+constexpr int kTN = 32;  // key slots per tile
+
 template <int KVT>
 struct TcCfg;
+// Staged bytes per slot: this CTA's latent half, and the row tail (FP8: the four block
+// scales and all 64 RoPE dims, 144 B; BF16: this CTA's 32 RoPE dims, 64 B).  A 4-row tail
+// gather lands on a 128-B aligned stride.
 template <>
 struct TcCfg<DCP_KV_FP8_E4M3_S128> {
-  static constexpr int TN = 16, NACC = 3, NS = 4, NK = 3, STG_LAT = 256, STG_SC = 16;
-  static constexpr int ROW_LAT = 256, ROW_ROPE = 528, ROW_SC = 512;  // byte offsets in a row
+  static constexpr int NACC = 2, NS = 4, NK = 3;
+  static constexpr int LAT_TOK = 256, TAIL_TOK = 144, TAIL_GSTRIDE = 640;
 };
 template <>
 struct TcCfg<DCP_KV_BF16> {
-  static constexpr int TN = 32, NACC = 1, NS = 3, NK = 3, STG_LAT = 512, STG_SC = 0;
-  static constexpr int ROW_LAT = 512, ROW_ROPE = 1024, ROW_SC = 0;
+  static constexpr int NACC = 1, NS = 3, NK = 3;
+  static constexpr int LAT_TOK = 512, TAIL_TOK = 64, TAIL_GSTRIDE = 256;
 };
 
 constexpr int kTcThreads = 384;
-constexpr int kColO = 0, kColQ = 256, kColS = 400;
+constexpr int kColO = 0, kColQ = 256, kColS = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kTwo56 = 72057594037927936.0f;  // 2^56
+constexpr float kScaleFloor = 8.67361737988403547e-19f;  // 2^-60
 
 template <int KVT>
 struct TcLay {
   using C = TcCfg<KVT>;
-  static constexpr int TN = C::TN;
-  static constexpr int BS = TN * 128;  // bytes between 64-dim column blocks of a K tile
-  static constexpr int KT_BYTES = 5 * BS;
-  static constexpr int STG_TOK = C::STG_LAT + 64 + C::STG_SC;
-  static constexpr int STG_BYTES = TN * STG_TOK;
-  static constexpr int XSTRIDE = TN + 4;  // floats per exchange row (16-B aligned rows)
+  static constexpr int TN = kTN;
+  static constexpr int BS = TN * 128;        // bytes between 64-dim column blocks of a K tile
+  static constexpr int KT_BYTES = 5 * BS;    // 4 latent blocks + 1 RoPE block
+  static constexpr int STG_TAIL = TN * C::LAT_TOK;
+  static constexpr int STG_BYTES = STG_TAIL + (TN / 4) * C::TAIL_GSTRIDE;
+  static constexpr int GROUP_TX = 4 * (C::LAT_TOK + C::TAIL_TOK);  // bytes of one 4-row group
+  static constexpr int QR_BYTES = 128 * 128;  // RoPE part of Q: 128 rows of one SW128 row
+  static constexpr int XSTRIDE = TN + 4;      // floats per exchange row (16-B aligned rows)
   static constexpr int X_BYTES = 128 * XSTRIDE * 4;
-  static constexpr int META_BYTES = 16 + TN * 8;
+  // per K tile: mask | logit scale lo | logit scale hi | P scale lo | P scale hi
+  static constexpr int META_BYTES = 16 + 4 * TN * 4;
   static constexpr int SBUF = C::NACC * TN;
   static constexpr int OFF_KT = 0;
   static constexpr int OFF_STG = OFF_KT + C::NK * KT_BYTES;
-  static constexpr int OFF_X = OFF_STG + C::NS * STG_BYTES;
+  static constexpr int OFF_QR = OFF_STG + C::NS * STG_BYTES;
+  static constexpr int OFF_X = OFF_QR + QR_BYTES;
   static constexpr int OFF_META = OFF_X + 2 * X_BYTES;
   static constexpr int OFF_END = OFF_META + C::NK * META_BYTES;
   // at least 120 KB so that one CTA (and one TMEM owner) sits on an SM
   static constexpr int SMEM = (OFF_END + 1024 > 122880 ? OFF_END + 1024 : 122880);
+  static_assert(OFF_STG % 1024 == 0 && STG_BYTES % 1024 == 0 && OFF_QR % 1024 == 0,
+                "SW128 tiles and TMA destinations need 1024-B / 128-B alignment");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(kColS + 2 * SBUF <= (int)kTmemCols, "TMEM columns");
 };
 
 struct TcShared {
@@ -93,6 +112,7 @@ struct TcShared {
   uint64_t s_full[2], p_full[2], pv_done[2], q_ready, in_full[2], out_free[2], drain;
   uint64_t fin_pub, fin_dec;  // split-unit publish / merge decision
   uint32_t stg_mask[4];
+  uint32_t stg_issued[4];     // gathers issued per staging slot (for the teardown wait)
   uint32_t tmem_base;
   int abort_flag;
   int last_flag;
@@ -109,7 +129,7 @@ struct UnitInfo {
   int shard, b, n, ntile;
 };
 
-template <bool FUSED, bool SPARSE, int TN>
+template <bool FUSED, bool SPARSE>
 __device__ __forceinline__ UnitInfo get_unit(const DecodeParams& p, int64_t u) {
   UnitInfo x;
   x.r = FUSED ? u : u % p.rows;
@@ -120,12 +140,12 @@ __device__ __forceinline__ UnitInfo get_unit(const DecodeParams& p, int64_t u) {
   else
     x.n = max(0, __ldg(p.kv_len + u));
   if (x.b < 0 || x.b >= p.num_seqs) x.n = 0;
-  x.ntile = (x.n + TN - 1) / TN;
+  x.ntile = (x.n + kTN - 1) / kTN;
   return x;
 }
 
 // Walk over this pair's tiles, unit by unit (empty units contribute no tiles).
-template <bool FUSED, bool SPARSE, int TN>
+template <bool FUSED, bool SPARSE>
 struct Walk {
   int64_t u;
   int lt, left;
@@ -134,7 +154,7 @@ struct Walk {
     u = u0;
     lt = tile0;
     left = ntiles;
-    if (left > 0) info = get_unit<FUSED, SPARSE, TN>(p, u);
+    if (left > 0) info = get_unit<FUSED, SPARSE>(p, u);
   }
   __device__ bool first() const { return lt == 0; }
   __device__ bool last() const { return lt == info.ntile - 1; }
@@ -143,47 +163,12 @@ struct Walk {
     if (++lt == info.ntile) {
       do {
         ++u;
-        info = get_unit<FUSED, SPARSE, TN>(p, u);
+        info = get_unit<FUSED, SPARSE>(p, u);
       } while (info.ntile == 0);
       lt = 0;
     }
   }
 };
-
-// Global pool row of token position `pos` of the unit, or nullptr (padding / out of range).
-template <int KVT, bool FUSED, bool SPARSE>
-__device__ __forceinline__ const uint8_t* tc_resolve(const DecodeParams& p, const UnitInfo& x,
-                                                     int64_t u, int pos) {
-  if (pos >= x.n) return nullptr;
-  int l;
-  const int32_t* table;
-  if (FUSED) {
-    const int t = SPARSE ? __ldg(p.idx + x.r * (int64_t)p.k + pos) : pos;
-    if (t < 0) return nullptr;
-    const int s = owner_of(t, p.D, p.I);
-    l = local_of(t, p.D, p.I);
-    table = p.bt + ((int64_t)s * p.num_seqs + x.b) * p.bt_stride;
-  } else {
-    l = SPARSE ? __ldg(p.idx + u * (int64_t)p.k + pos) : pos;
-    if (l < 0) {
-      set_err(p.err, DCP_ERRBIT_SLOT_RANGE);
-      return nullptr;
-    }
-    table = p.bt + ((int64_t)x.shard * p.num_seqs + x.b) * p.bt_stride;
-  }
-  const int pj = l >> 6;  // page size 64
-  if (pj >= p.bt_stride) {
-    set_err(p.err, DCP_ERRBIT_SLOT_RANGE);
-    return nullptr;
-  }
-  const int page = __ldg(table + pj);
-  if (page < 0 || page >= p.num_pages) {
-    set_err(p.err, DCP_ERRBIT_PAGE_RANGE);
-    return nullptr;
-  }
-  constexpr int tb = KVT == DCP_KV_BF16 ? kTokBytesBF16 : kTokBytesFP8;
-  return p.pool + ((int64_t)page * 64 + (l & 63)) * tb;
-}
 
 // Block-wide exclusive prefix of v (384 threads); returns the prefix, *total the sum.
 __device__ __forceinline__ int64_t block_scan_excl(int64_t v, TcShared& sh, int64_t* total) {
@@ -206,12 +191,19 @@ __device__ __forceinline__ int64_t block_scan_excl(int64_t v, TcShared& sh, int6
   return base + x - v;
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+
 template <int KVT, bool FUSED, bool SPARSE>
 __global__ void __launch_bounds__(kTcThreads, 1)
-decode_tc_kernel(const DecodeParams p) {
+decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_lat,
+                 const __grid_constant__ CUtensorMap tm_tail) {
   using C = TcCfg<KVT>;
   using L = TcLay<KVT>;
-  constexpr int TN = C::TN, NS = C::NS, NK = C::NK;
+  constexpr int TN = kTN, NS = C::NS, NK = C::NK;
+  constexpr bool FP8 = KVT == DCP_KV_FP8_E4M3_S128;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -233,8 +225,9 @@ decode_tc_kernel(const DecodeParams p) {
   }
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sh.stg_full[i], 33);  // 32 copy-completion arrivals + 1 mask publication
+      mbar_init(&sh.stg_full[i], 1);  // the loader's expect-tx arrival; bytes from the gathers
       mbar_init(&sh.stg_empty[i], 4);
+      sh.stg_issued[i] = 0;
     }
     for (int i = 0; i < NK; ++i) {
       mbar_init(&sh.kt_full[i], 4);
@@ -275,7 +268,7 @@ decode_tc_kernel(const DecodeParams p) {
     }
   } else {
     int64_t part = 0;
-    for (int64_t u = tid; u < U; u += kTcThreads) part += get_unit<FUSED, SPARSE, TN>(p, u).ntile;
+    for (int64_t u = tid; u < U; u += kTcThreads) part += get_unit<FUSED, SPARSE>(p, u).ntile;
     int64_t T;
     block_scan_excl(part, sh, &T);
     const int Pe = (int)(T < P ? (T > 0 ? T : 1) : P);
@@ -293,7 +286,7 @@ decode_tc_kernel(const DecodeParams p) {
     if (t1 > t0) {
       for (int64_t c0 = 0; c0 < U; c0 += kTcThreads) {
         const int64_t u = c0 + tid;
-        const int nt = u < U ? get_unit<FUSED, SPARSE, TN>(p, u).ntile : 0;
+        const int nt = u < U ? get_unit<FUSED, SPARSE>(p, u).ntile : 0;
         int64_t chunk_total;
         const int64_t excl = block_scan_excl(nt, sh, &chunk_total) + sh.scan_base;
         if (nt > 0 && t0 >= excl && t0 < excl + nt) {
@@ -317,16 +310,20 @@ decode_tc_kernel(const DecodeParams p) {
 
   if (warp >= 1 && warp <= 3) {
     // ============================================================ loaders
-    // Warp 1+li takes tiles j = li, li+3, ...  A three-stage software pipeline hides the
-    // dependent loads: stage I loads the tile's slot ids (two tiles of this warp ahead),
-    // stage T maps them to owner shard / local slot and loads the block-table entry (one
-    // tile ahead), stage C turns pages into row addresses and issues 16-B cp.async copies
-    // of this CTA's share of each row into the staging slot.
+    // Warp 1+li takes tiles j = li, li+3, ...; lane t handles slot t of a tile.  Stage I
+    // loads the tile's slot ids (two tiles of this warp ahead), stage T maps them to owner
+    // shard / local slot and loads the block-table entry (one tile ahead), stage C turns
+    // pages into pool rows and issues one latent and one tail gather per 4 slots.
     constexpr int NLD = 3;
-    constexpr int CH_LAT = C::STG_LAT / 16, CH = CH_LAT + 4 + C::STG_SC / 16;
-    constexpr int tb = KVT == DCP_KV_BF16 ? kTokBytesBF16 : kTokBytesFP8;
     const int li = warp - 1;
-    Walk<FUSED, SPARSE, TN> wi;
+    if (li == 0 && lane == 0) {
+      prefetch_tensormap(&tm_lat);
+      prefetch_tensormap(&tm_tail);
+    }
+    // gather column offsets (elements of the map: bytes for FP8, bf16 for BF16)
+    const int xa = (int)crank * 256;
+    const int xb = FP8 ? 512 : 512 + 32 * (int)crank;
+    Walk<FUSED, SPARSE> wi;
     wi.init(p, sh.unit0, sh.tile0, ntiles);
     for (int k = 0; k < li && k + 1 < ntiles; ++k) wi.next(p);
     int t_v = -1;                   // stage T: slot id (global, local, or position)
@@ -339,41 +336,38 @@ decode_tc_kernel(const DecodeParams p) {
       if (jc >= 0) {
         const int slot = jc % NS;
         if (!mbar_wait(&sh.stg_empty[slot], ((jc / NS) & 1) ^ 1, abort_flag)) break;
-        const uint8_t* row = nullptr;
+        int row = -1;
         if (c_l >= 0) {
           if (c_page >= 0 && c_page < p.num_pages)
-            row = p.pool + ((int64_t)c_page * 64 + (c_l & 63)) * tb;
+            row = c_page * 64 + (c_l & 63);  // < 2^31: the host checks num_pages * 64
           else
             set_err(p.err, DCP_ERRBIT_PAGE_RANGE);
         }
-        const unsigned mask = __ballot_sync(0xffffffffu, row != nullptr);
+        const unsigned mask = __ballot_sync(0xffffffffu, row >= 0);
+        // empty positions of a 4-slot group re-read a valid row of the group (their data
+        // is replaced by zeros in the converter); groups without any row are not fetched
+        const unsigned quad = (mask >> (lane & ~3)) & 0xFu;
+        const int sub = __shfl_sync(0xffffffffu, row, (lane & ~3) + (quad ? __ffs(quad) - 1 : 0));
+        const int rowfix = row >= 0 ? row : sub;
+        const int g = lane & 7;
+        const int y0 = __shfl_sync(0xffffffffu, rowfix, 4 * g);
+        const int y1 = __shfl_sync(0xffffffffu, rowfix, 4 * g + 1);
+        const int y2 = __shfl_sync(0xffffffffu, rowfix, 4 * g + 2);
+        const int y3 = __shfl_sync(0xffffffffu, rowfix, 4 * g + 3);
+        const bool gnz = ((mask >> (4 * g)) & 0xFu) != 0;
+        const unsigned gmask = __ballot_sync(0xffffffffu, lane < 8 && gnz);
         unsigned char* stg = smem + L::OFF_STG + slot * L::STG_BYTES;
-        const unsigned long long rowv = reinterpret_cast<unsigned long long>(row);
-#pragma unroll 4
-        for (int it = 0; it < (TN * CH + 31) / 32; ++it) {
-          const int c = it * 32 + lane;
-          const int tok = min(c / CH, TN - 1), sub = c - tok * CH;
-          const uint8_t* r = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, rowv, tok));
-          if (c < TN * CH && r != nullptr) {
-            const uint8_t* src;
-            unsigned char* dst;
-            if (sub < CH_LAT) {
-              src = r + crank * C::ROW_LAT + sub * 16;
-              dst = stg + tok * C::STG_LAT + sub * 16;
-            } else if (sub < CH_LAT + 4) {
-              src = r + C::ROW_ROPE + crank * 64 + (sub - CH_LAT) * 16;
-              dst = stg + TN * C::STG_LAT + tok * 64 + (sub - CH_LAT) * 16;
-            } else {
-              src = r + C::ROW_SC;
-              dst = stg + TN * (C::STG_LAT + 64) + tok * 16;
-            }
-            cp_async16(dst, src);
-          }
+        if (lane == 0) {
+          sh.stg_mask[slot] = mask;
+          sh.stg_issued[slot] += 1;
+          mbar_arrive_expect_tx(&sh.stg_full[slot], __popc(gmask) * L::GROUP_TX);
         }
-        if (lane == 0) sh.stg_mask[slot] = mask;
         __syncwarp();
-        cp_async_arrive_noinc(&sh.stg_full[slot]);     // when this lane's copies land
-        if (lane == 0) mbar_arrive(&sh.stg_full[slot]);  // publishes the mask
+        if (lane < 8 && gnz) {
+          tma_gather4(stg + g * 4 * C::LAT_TOK, &tm_lat, xa, y0, y1, y2, y3, &sh.stg_full[slot]);
+          tma_gather4(stg + L::STG_TAIL + g * C::TAIL_GSTRIDE, &tm_tail, xb, y0, y1, y2, y3,
+                      &sh.stg_full[slot]);
+        }
       }
       // stage T for tile jt
       int n_page = -1, n_l = -1;
@@ -402,7 +396,7 @@ decode_tc_kernel(const DecodeParams p) {
       int n_v = -1;
       bool n_has = false;
       const UnitInfo n_x = wi.info;
-      if (ji < ntiles && lane < TN) {
+      if (ji < ntiles) {
         const int pos = wi.lt * TN + lane;
         if (pos < wi.info.n) {
           n_has = true;
@@ -422,13 +416,12 @@ decode_tc_kernel(const DecodeParams p) {
       t_has = n_has;
       t_x = n_x;
     }
-    cp_async_wait_all();  // no copy in flight when the CTA winds down
   } else if (warp == 0) {
     // ============================================================ MMA issuer
     constexpr uint32_t idesc_qk = idesc_bf16(128, TN, 0, 0);
-    constexpr uint32_t idesc_pv = KVT == DCP_KV_BF16 ? idesc_bf16(128, 256, 0, 1)
-                                                     : idesc_bf16(128, 128, 0, 1);
+    constexpr uint32_t idesc_pv = FP8 ? idesc_bf16(128, 128, 0, 1) : idesc_bf16(128, 256, 0, 1);
     const uint32_t qb = tbase + kColQ;
+    const uint64_t qrd = smem_desc(smem_u32(smem + L::OFF_QR), 16, 1024);
     const uint32_t leader = elect_one();
     int q_phase = 0;
     bool ok = true;
@@ -447,21 +440,31 @@ decode_tc_kernel(const DecodeParams p) {
         const uint32_t kt = smem_u32(smem + L::OFF_KT + (j % NK) * L::KT_BYTES);
         const uint32_t sb = tbase + kColS + (j & 1) * L::SBUF;
         const uint64_t kd = smem_desc(kt, 16, 1024);
+        // start-address field (address >> 4) of K-step ks of the latent blocks / the RoPE block
+#define KOFF(ks) ((uint64_t)((((ks) >> 2) * L::BS + ((ks) & 3) * 32) >> 4))
+#define ROFF(i) ((uint64_t)((4 * L::BS + (i) * 32) >> 4))
+        if (FP8) {
+          // the two latent-block chains interleaved (consecutive MMAs write different
+          // accumulators), then the RoPE high parts and remainders into the lo chain
 #pragma unroll
-        for (int i = 0; i < 18; ++i) {
-          // FP8: the two latent-block chains are interleaved so that consecutive MMAs
-          // write different accumulators
-          const int ks = KVT == DCP_KV_BF16 ? i : (i < 16 ? (i >> 1) + 8 * (i & 1) : i);
-          // start-address field (bits 0-13, address >> 4) of a constant offset from kd
-          const uint64_t bd = kd + (uint64_t)((((ks >> 2) * L::BS + (ks & 3) * 32)) >> 4);
-          if (KVT == DCP_KV_BF16) {
-            mma_ts_if(leader, sb, qb + 8 * ks, bd, idesc_qk, ks > 0);
-          } else {
-            const int acc = ks < 8 ? 0 : ks < 16 ? 1 : 2;
-            const int k0 = acc * 8;
-            mma_ts_if(leader, sb + acc * TN, qb + 8 * ks, bd, idesc_qk, ks > k0);
+          for (int i = 0; i < 16; ++i) {
+            const int ks = (i >> 1) + 8 * (i & 1);
+            mma_ts_if(leader, sb + (i & 1) * TN, qb + 8 * ks, kd + KOFF(ks), idesc_qk,
+                      (ks & 7) != 0);
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            mma_ss_if(leader, sb, qrd + (uint64_t)(((i & 1) * 32) >> 4), kd + ROFF(i), idesc_qk, 1);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < 16; ++ks)
+            mma_ts_if(leader, sb, qb + 8 * ks, kd + KOFF(ks), idesc_qk, ks > 0);
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+            mma_ss_if(leader, sb, qrd + (uint64_t)((i * 32) >> 4), kd + ROFF(i), idesc_qk, 1);
         }
+#undef KOFF
+#undef ROFF
         mma_commit_if(leader, &sh.s_full[j & 1]);
       }
       return true;
@@ -469,7 +472,7 @@ decode_tc_kernel(const DecodeParams p) {
     // Q.K^T runs two tiles ahead of P.V: QK(j+2) overwrites S buffer j&1, which needs
     // A(j) to have read S(j) (implied by p_full(j-1)) and P.V(j-1) to have read P(j-1)
     // (waited for in issue_qk); for j = 0 the first condition is only known after p_full(0).
-    Walk<FUSED, SPARSE, TN> w, wq;
+    Walk<FUSED, SPARSE> w, wq;
     w.init(p, sh.unit0, sh.tile0, ntiles);
     wq = w;
     // the softmax warps load Q for the pair's first unit even when it starts mid-unit
@@ -490,15 +493,16 @@ decode_tc_kernel(const DecodeParams p) {
         const uint32_t sb = tbase + kColS + ((j + 1) & 1) * L::SBUF;  // P(j)
         // a unit's (or this pair's) first tile overwrites O
         const uint32_t acc0 = (w.first() || j == 0) ? 0u : 1u;
-        if (KVT == DCP_KV_BF16) {
-#pragma unroll
-          for (int kk = 0; kk < TN / 16; ++kk)
-            mma_ts_if(leader, tbase + kColO, sb + 8 * kk, smem_desc(kt + kk * 2048, L::BS, 1024),
-                      idesc_pv, acc0 | (kk > 0));
+        if (FP8) {  // P_lo = cols [0,16) (slots 0-15, 16-31), P_hi = cols [16,32)
+          mma_ts_if(leader, tbase + kColO, sb, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
+          mma_ts_if(leader, tbase + kColO + 128, sb + 16, smem_desc(kt + 2 * L::BS, L::BS, 1024),
+                    idesc_pv, acc0);
+          mma_ts_if(leader, tbase + kColO, sb + 8, smem_desc(kt + 2048, L::BS, 1024), idesc_pv, 1);
+          mma_ts_if(leader, tbase + kColO + 128, sb + 24,
+                    smem_desc(kt + 2 * L::BS + 2048, L::BS, 1024), idesc_pv, 1);
         } else {
           mma_ts_if(leader, tbase + kColO, sb, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
-          mma_ts_if(leader, tbase + kColO + 128, sb + TN / 2,
-                    smem_desc(kt + 2 * L::BS, L::BS, 1024), idesc_pv, acc0);
+          mma_ts_if(leader, tbase + kColO, sb + 8, smem_desc(kt + 2048, L::BS, 1024), idesc_pv, 1);
         }
         mma_commit_if(leader, &sh.kt_empty[j % NK]);
         mma_commit_if(leader, &sh.pv_done[j & 1]);
@@ -515,6 +519,7 @@ decode_tc_kernel(const DecodeParams p) {
   } else if (warp >= 4 && warp < 8) {
     // ============================================================ converters
     const int ct = tid - 128;
+    const float sl2 = p.scale_log2;
     for (int j = 0; j < ntiles; ++j) {
       const int slot = j % NS, ks = j % NK;
       if (!mbar_wait(&sh.stg_full[slot], (j / NS) & 1, abort_flag)) break;
@@ -524,18 +529,20 @@ decode_tc_kernel(const DecodeParams p) {
       unsigned char* kt = smem + L::OFF_KT + ks * L::KT_BYTES;
       unsigned char* meta = smem + L::OFF_META + ks * L::META_BYTES;
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-      if (KVT == DCP_KV_FP8_E4M3_S128) {
-        for (int q = ct; q < TN * 16; q += 128) {  // 16 codes per chunk
+      if (FP8) {
+#pragma unroll
+        for (int it = 0; it < TN * 16 / 128; ++it) {  // 16 codes per item
+          const int q = ct + 128 * it;
           const int t = q >> 4, ch = q & 15;
           const uint4 v = (mask >> t) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + t * 256 + ch * 16)
+                              ? *reinterpret_cast<const uint4*>(stg + t * C::LAT_TOK + ch * 16)
                               : zero;
           const uint32_t in[4] = {v.x, v.y, v.z, v.w};
           uint32_t o[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            o[2 * e] = e4m3x2_to_bf16x2_scaled((uint16_t)(in[e] & 0xffffu));
-            o[2 * e + 1] = e4m3x2_to_bf16x2_scaled((uint16_t)(in[e] >> 16));
+            o[2 * e] = e4m3x2_to_bf16x2((uint16_t)(in[e] & 0xffffu));
+            o[2 * e + 1] = e4m3x2_to_bf16x2((uint16_t)(in[e] >> 16));
           }
           unsigned char* base = kt + (ch >> 2) * L::BS + t * 128;
           const int c16 = (ch & 3) * 2;
@@ -543,33 +550,54 @@ decode_tc_kernel(const DecodeParams p) {
           *reinterpret_cast<uint4*>(base + (((c16 + 1) ^ (t & 7)) << 4)) =
               make_uint4(o[4], o[5], o[6], o[7]);
         }
-        if (ct < TN * 4) {  // RoPE half: 32 bf16 = 4 chunks per slot
+        {  // RoPE: thread -> (slot t, 8 of this CTA's 32 dims); scales
           const int t = ct >> 2, c4 = ct & 3;
-          const uint4 v = (mask >> t) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + TN * 256 + t * 64 + c4 * 16)
-                              : zero;
-          *reinterpret_cast<uint4*>(kt + 4 * L::BS + t * 128 + ((c4 ^ (t & 7)) << 4)) = v;
-        }
-        if (ct < TN) {  // this CTA's two block scales, premultiplied by 2^56
-          float2 sc = make_float2(0.f, 0.f);
-          if ((mask >> ct) & 1) {
-            const float4 s4 = *reinterpret_cast<const float4*>(stg + TN * (256 + 64) + ct * 16);
-            sc = crank == 0 ? make_float2(s4.x, s4.y) : make_float2(s4.z, s4.w);
+          const unsigned char* tail = stg + L::STG_TAIL + (t >> 2) * C::TAIL_GSTRIDE + (t & 3) * C::TAIL_TOK;
+          uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+          float slo = 0.f, shi = 0.f, sf = 1.f;
+          if ((mask >> t) & 1) {
+            const float4 sc = *reinterpret_cast<const float4*>(tail);
+            slo = crank == 0 ? sc.x : sc.z;
+            shi = crank == 0 ? sc.y : sc.w;
+            sf = fabsf(slo) < kScaleFloor ? kScaleFloor : slo;
+            const float inv = 1.0f / sf;
+            const uint4 r = *reinterpret_cast<const uint4*>(tail + 16 + 64 * crank + 16 * c4);
+            const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float y0 = __uint_as_float(rw[e] << 16) * inv;
+              const float y1 = __uint_as_float(rw[e] & 0xffff0000u) * inv;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(y0, y1);
+              hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
+              lw[e] = pack_bf16x2(y0 - __low2float(h2), y1 - __high2float(h2));
+            }
           }
-          reinterpret_cast<float2*>(meta + 16)[ct] = make_float2(sc.x * kTwo56, sc.y * kTwo56);
+          unsigned char* rb = kt + 4 * L::BS + t * 128;
+          *reinterpret_cast<uint4*>(rb + ((c4 ^ (t & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(rb + (((4 + c4) ^ (t & 7)) << 4)) =
+              make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          if (c4 == 0) {
+            float* mf = reinterpret_cast<float*>(meta + 16);
+            mf[t] = sf * sl2;
+            mf[TN + t] = shi * sl2;
+            mf[2 * TN + t] = slo;
+            mf[3 * TN + t] = shi;
+          }
         }
       } else {
-        for (int q = ct; q < TN * 32; q += 128) {  // 8 bf16 per chunk
+#pragma unroll
+        for (int it = 0; it < TN * 32 / 128; ++it) {  // 8 bf16 per item
+          const int q = ct + 128 * it;
           const int t = q >> 5, ch = q & 31;
           const uint4 v = (mask >> t) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + t * 512 + ch * 16)
+                              ? *reinterpret_cast<const uint4*>(stg + t * C::LAT_TOK + ch * 16)
                               : zero;
           *reinterpret_cast<uint4*>(kt + (ch >> 3) * L::BS + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = v;
         }
         {
           const int t = ct >> 2, c4 = ct & 3;
           const uint4 v = (mask >> t) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + TN * 512 + t * 64 + c4 * 16)
+                              ? *reinterpret_cast<const uint4*>(stg + L::STG_TAIL + t * C::TAIL_TOK + c4 * 16)
                               : zero;
           *reinterpret_cast<uint4*>(kt + 4 * L::BS + t * 128 + ((c4 ^ (t & 7)) << 4)) = v;
         }
@@ -593,7 +621,7 @@ decode_tc_kernel(const DecodeParams p) {
     // units without any slot: zero output, -inf LSE
     if (!(FUSED && SPARSE)) {
       for (int64_t u = pair; u < U; u += P) {
-        const UnitInfo x = get_unit<FUSED, SPARSE, TN>(p, u);
+        const UnitInfo x = get_unit<FUSED, SPARSE>(p, u);
         if (x.ntile != 0 || h >= H) continue;
         const int64_t oi = (u * H + h) * kDv + crank * 256;
         if (FUSED) {
@@ -607,26 +635,36 @@ decode_tc_kernel(const DecodeParams p) {
       }
     }
 
+    // Q of row r: this CTA's 256 latent dims into TMEM (two bf16 per column), its 32 RoPE
+    // dims into row h of the SW128 A-operand tile in shared memory
     auto load_q = [&](int64_t r) {
-      uint32_t w[16];
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) + (r * H + h) * kDqk);
-      for (int c = 0; c < 9; ++c) {  // 8 chunks of latent (4 x uint4 each) + 1 of RoPE
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (h < H) v = __ldg(src + (c < 8 ? crank * 32 + c * 4 + i : 64 + crank * 4 + i));
+          if (h < H) v = __ldg(src + crank * 32 + c * 4 + i);
           w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
         tmem_st16(trow + kColQ + 16 * c, w);
       }
+      unsigned char* qr = smem + L::OFF_QR + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (h < H) v = __ldg(src + 64 + crank * 4 + i);
+        *reinterpret_cast<uint4*>(qr + ((i ^ (h & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.q_ready);
     };
 
-    Walk<FUSED, SPARSE, TN> w;
+    Walk<FUSED, SPARSE> w;
     w.init(p, sh.unit0, sh.tile0, ntiles);
     if (ntiles > 0) load_q(w.info.r);
     float m_ref = -INFINITY, lsum = 0.f;
@@ -641,8 +679,7 @@ decode_tc_kernel(const DecodeParams p) {
       volatile int no_abort = 0;
       mbar_wait(&sh.pv_done[jl & 1], (jl >> 1) & 1, ok ? abort_flag : &no_abort);
       tc_fence_after();
-      const float inv = lsum > 0.f ? 1.0f / lsum : 0.f;
-      const float fix = (KVT == DCP_KV_BF16 ? 1.0f : kTwo56) * inv;
+      const float fix = lsum > 0.f ? 1.0f / lsum : 0.f;
       const float lse_v = lsum > 0.f ? (m_ref + __log2f(lsum)) * kLn2 : -INFINITY;
       const int64_t u = w.u;
       const int64_t oi = (u * H + h) * kDv + crank * 256;
@@ -663,10 +700,7 @@ decode_tc_kernel(const DecodeParams p) {
           if (FUSED) {
             uint32_t b2[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              __nv_bfloat162 t2 = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-              b2[i] = *reinterpret_cast<uint32_t*>(&t2);
-            }
+            for (int i = 0; i < 8; ++i) b2[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
             uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
             o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
             o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
@@ -742,10 +776,7 @@ decode_tc_kernel(const DecodeParams p) {
           if (FUSED) {
             uint32_t b2[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              __nv_bfloat162 t2 = __floats2bfloat162_rn(acc[2 * i] * iw, acc[2 * i + 1] * iw);
-              b2[i] = *reinterpret_cast<uint32_t*>(&t2);
-            }
+            for (int i = 0; i < 8; ++i) b2[i] = pack_bf16x2(acc[2 * i] * iw, acc[2 * i + 1] * iw);
             uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
             o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
             o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
@@ -765,41 +796,43 @@ decode_tc_kernel(const DecodeParams p) {
     // peer.  Stage B(j): add the peer's partial, online softmax, P into TMEM, finish the
     // unit.  Order A(0), A(1), B(0), A(2), B(1), ...: tile j's exchange is in flight while
     // A(j+1) runs, so the DSMEM round trip leaves the critical path.
-    auto stage_a = [&](int j, const Walk<FUSED, SPARSE, TN>& wa, float (&s)[TN]) -> bool {
+    auto stage_a = [&](int j, const Walk<FUSED, SPARSE>& wa, float (&s)[TN]) -> bool {
       const int buf = j & 1;
       if (!mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag)) return false;
       if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) return false;
       tc_fence_after();
       const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
-      const float2* scl = reinterpret_cast<const float2*>(meta + 16);
       const uint32_t sb = trow + kColS + buf * L::SBUF;
-      uint32_t a[TN];
-      if (TN == 32) {
+      if (!FP8) {
+        uint32_t a[TN];
         tmem_ld16(sb, a);
         tmem_ld16(sb + 16, a + 16);
-      } else {
-        tmem_ld16(sb, a);
-      }
-      if (KVT == DCP_KV_BF16) {
         tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * sl2;
       } else {
-        uint32_t b[TN], r[TN];
-        tmem_ld16(sb + TN, b);
-        tmem_ld16(sb + 2 * TN, r);
-        tmem_ld_wait();
+        const float4* ma = reinterpret_cast<const float4*>(meta + 16);
+        const float4* mb = ma + TN / 4;
 #pragma unroll
-        for (int t = 0; t < TN; ++t) {
-          const float2 sc = scl[t];
-          const float x = fmaf(__uint_as_float(a[t]) * kTwo56, sc.x,
-                               fmaf(__uint_as_float(b[t]) * kTwo56, sc.y, __uint_as_float(r[t])));
-          s[t] = x * sl2;
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t lo[16], hi[16];
+          tmem_ld16(sb + 16 * hf, lo);
+          tmem_ld16(sb + TN + 16 * hf, hi);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            const float4 a = ma[4 * hf + t4], b = mb[4 * hf + t4];
+            const int t = 16 * hf + 4 * t4;
+            s[t] = fmaf(__uint_as_float(lo[4 * t4]), a.x, __uint_as_float(hi[4 * t4]) * b.x);
+            s[t + 1] = fmaf(__uint_as_float(lo[4 * t4 + 1]), a.y, __uint_as_float(hi[4 * t4 + 1]) * b.y);
+            s[t + 2] = fmaf(__uint_as_float(lo[4 * t4 + 2]), a.z, __uint_as_float(hi[4 * t4 + 2]) * b.z);
+            s[t + 3] = fmaf(__uint_as_float(lo[4 * t4 + 3]), a.w, __uint_as_float(hi[4 * t4 + 3]) * b.w);
+          }
         }
       }
-      // the next unit's queries go into TMEM once this tile's Q.K^T is done
+      // the next unit's queries go in once this tile's Q.K^T is done
       if (wa.last() && j + 1 < ntiles) {
-        Walk<FUSED, SPARSE, TN> wn = wa;
+        Walk<FUSED, SPARSE> wn = wa;
         wn.next(p);
         load_q(wn.info.r);
       }
@@ -818,15 +851,13 @@ decode_tc_kernel(const DecodeParams p) {
     if (ntiles > 0) ok = stage_a(0, w, s_cur);
     for (; ok && j < ntiles; ++j) {
       if (j + 1 < ntiles) {
-        Walk<FUSED, SPARSE, TN> wn = w;
+        Walk<FUSED, SPARSE> wn = w;
         wn.next(p);
         if (!(ok = stage_a(j + 1, wn, s_nxt))) break;
       }
       // ---- stage B(j)
-      const int buf = j & 1;
       const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
       const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
-      const float2* scl = reinterpret_cast<const float2*>(meta + 16);
       // P(j) goes into S buffer (j+1)&1: A(j+1) has already read S(j+1) out of it, and
       // P(j-2), which it held before, has been read by P.V(j-2) (waited for below)
       const uint32_t sb = trow + kColS + ((j + 1) & 1) * L::SBUF;
@@ -884,32 +915,31 @@ decode_tc_kernel(const DecodeParams p) {
       }
       if (j >= 2 && !(ok = mbar_wait(&sh.pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag))) break;
       tc_fence_after();
-      if (KVT == DCP_KV_BF16) {
+      if (!FP8) {
         uint32_t pw[TN / 2];
 #pragma unroll
-        for (int i = 0; i < TN / 2; ++i) {
-          __nv_bfloat162 t2 = __floats2bfloat162_rn(pr[2 * i], pr[2 * i + 1]);
-          pw[i] = *reinterpret_cast<uint32_t*>(&t2);
-        }
+        for (int i = 0; i < TN / 2; ++i) pw[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
         tmem_st16(sb, pw);
       } else {
+        const float4* pl4 = reinterpret_cast<const float4*>(meta + 16 + 8 * TN);
+        const float4* ph4 = pl4 + TN / 4;
         uint32_t plo[TN / 2], phi[TN / 2];
 #pragma unroll
-        for (int i = 0; i < TN / 2; ++i) {
-          const float2 s0 = scl[2 * i], s1 = scl[2 * i + 1];
-          __nv_bfloat162 a2 = __floats2bfloat162_rn(pr[2 * i] * s0.x, pr[2 * i + 1] * s1.x);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(pr[2 * i] * s0.y, pr[2 * i + 1] * s1.y);
-          plo[i] = *reinterpret_cast<uint32_t*>(&a2);
-          phi[i] = *reinterpret_cast<uint32_t*>(&b2);
+        for (int i = 0; i < TN / 4; ++i) {
+          const float4 a = pl4[i], b = ph4[i];
+          plo[2 * i] = pack_bf16x2(pr[4 * i] * a.x, pr[4 * i + 1] * a.y);
+          plo[2 * i + 1] = pack_bf16x2(pr[4 * i + 2] * a.z, pr[4 * i + 3] * a.w);
+          phi[2 * i] = pack_bf16x2(pr[4 * i] * b.x, pr[4 * i + 1] * b.y);
+          phi[2 * i + 1] = pack_bf16x2(pr[4 * i + 2] * b.z, pr[4 * i + 3] * b.w);
         }
-        tmem_st8(sb, plo);
-        tmem_st8(sb + TN / 2, phi);
+        tmem_st16(sb, plo);
+        tmem_st16(sb + TN / 2, phi);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&sh.p_full[buf]);
+        mbar_arrive(&sh.p_full[j & 1]);
         // this warp's inbox rows were read (and used) above: a relaxed arrive suffices
         mbar_arrive_cluster_relaxed(&sh.out_free[x], peer);
       }
@@ -933,6 +963,14 @@ decode_tc_kernel(const DecodeParams p) {
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
+  if (tid == 0 && sh.abort_flag) {
+    // an aborted CTA may still have gathers in flight into its staging ring: wait for the
+    // last one issued into each slot (nothing is issued into a slot before the previous
+    // gather there has landed, so only that one can be pending)
+    volatile int no_abort = 0;
+    for (int i = 0; i < NS; ++i)
+      if (sh.stg_issued[i] > 0) mbar_wait(&sh.stg_full[i], (sh.stg_issued[i] - 1) & 1, &no_abort);
+  }
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
@@ -975,12 +1013,60 @@ int tc_pairs_for(int64_t units, int64_t tiles_bound) {
   return (int)pairs;
 }
 
-int tc_tile_slots(int kv_dtype) { return kv_dtype == DCP_KV_BF16 ? 32 : 16; }
+int tc_tile_slots(int kv_dtype) {
+  (void)kv_dtype;
+  return kTN;
+}
 
 // DCPMLA_PATH=simt selects the CUDA-core path for every head count (read at each call).
 bool tc_path_enabled() {
   const char* e = getenv("DCPMLA_PATH");
   return !(e && e[0] == 's');
+}
+
+// The pool as a 2-D tensor [num_pages * 64 rows][row elements] for the 4-row gathers:
+// FP8 rows as 656 bytes (latent box 256 B, tail box 144 B from byte 512), BF16 rows as 576
+// bf16 (latent box 256 elements, RoPE box 32 elements).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+static cudaError_t make_pool_maps(const DecodeParams& p, int kv_dtype, CUtensorMap* lat,
+                                  CUtensorMap* tail) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const bool bf = kv_dtype == DCP_KV_BF16;
+  const CUtensorMapDataType dt = bf ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const cuuint64_t dims[2] = {bf ? 576ull : 656ull, (cuuint64_t)p.num_pages * 64};
+  const cuuint64_t strides[1] = {bf ? 1152ull : 656ull};
+  const cuuint32_t box_lat[2] = {256, 1};
+  const cuuint32_t box_tail[2] = {bf ? 32u : 144u, 1};
+  const cuuint32_t es[2] = {1, 1};
+  void* base = const_cast<uint8_t*>(p.pool);
+  if (enc(lat, dt, 2, base, dims, strides, box_lat, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (enc(tail, dt, 2, base, dims, strides, box_tail, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
 }
 
 template <int KVT, bool FUSED, bool SPARSE>
@@ -993,6 +1079,9 @@ static cudaError_t tc_launch_one(const DecodeParams& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  alignas(64) CUtensorMap lat, tail;
+  cudaError_t e = make_pool_maps(p, KVT, &lat, &tail);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * p.pairs, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
@@ -1005,7 +1094,7 @@ static cudaError_t tc_launch_one(const DecodeParams& p, cudaStream_t st) {
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return cudaLaunchKernelEx(&cfg, kern, p, lat, tail);
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,

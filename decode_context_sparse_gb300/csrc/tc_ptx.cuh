@@ -232,6 +232,14 @@ __device__ __forceinline__ void mma_ts_if(uint32_t leader, uint32_t d_tmem, uint
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
+__device__ __forceinline__ void mma_ss_if(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
+                                          uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 e, %5, 0;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_if(uint32_t leader, uint64_t* bar) {
   asm volatile(
       "{\n .reg .pred e;\n setp.ne.b32 e, %1, 0;\n"
@@ -265,6 +273,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Four-row TMA gather (2-D tensor map with a one-row box): rows y0..y3 of the tensor, box
+// columns [x, x + box width), land back to back at dst (128-B aligned); completion counted
+// in bytes on `bar`.  x * element size must be a multiple of 16 B.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int x, int y0, int y1,
+                                            int y2, int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
 // Per-thread 16-B asynchronous copy global -> shared (L2 only), tracked by cp.async groups.
@@ -314,6 +337,14 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint16_t codes) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
   return ((h2 >> 3) & 0x0FFF0FFFu) | (h2 & 0x80008000u);
+}
+// Two E4M3 codes -> two bf16 of the same values, exactly: the image above times 2^112 (a
+// power-of-two product that neither rounds nor leaves the normal range: |v| <= 448,
+// smallest non-zero 2^-9).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e4m3x2_to_bf16x2_scaled(codes)), "r"(0x77807780u));
+  return r;
 }
 
 }  // namespace tc
