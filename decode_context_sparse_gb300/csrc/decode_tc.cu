@@ -13,21 +13,26 @@
 // shared memory (st.async counted on the peer's mbarrier) and both CTAs run the same
 // softmax.
 //
-// Per CTA (384 threads), tiles of 32 key slots:
-//   warps 1-3   loaders (tiles round-robin): slot id -> owner shard / local slot -> page
+// Per CTA (512 threads), tiles of 32 key slots:
+//   warps 1-3   loaders (tiles round-robin; as many as staging slots, at most three):
+//               slot id -> owner shard / local slot -> page
 //               (a three-stage software pipeline over the dependent loads), then 4-row TMA
 //               gathers of this CTA's latent half and of the row tail into a staging ring;
 //   warp 0      TMEM owner and MMA issuer: S = Q K^T (latent part of Q in TMEM, RoPE part
-//               of Q in shared memory), then O += P V with P as the A operand in TMEM;
+//               of Q in shared memory) and O += P V (P in shared memory), each issued as
+//               soon as its inputs are ready;
 //   warps 4-7   converters: staging -> SWIZZLE_128B bf16 K tile (FP8: E4M3 -> bf16,
 //               exact), zero rows for padding, per-slot scales;
-//   warps 8-11  softmax: thread h owns head h (TMEM lane h): reads its logits, exchanges
-//               partial logits with the peer, online softmax in base 2 with a lazily
-//               raised reference max (the output is rescaled only when the max grows by
-//               more than 2^8), writes P as bf16 into TMEM, and at the end of a row
-//               normalises O and writes it out (or merges split rows).
-// TMEM columns: O [0,256) | Q latent [256,384) | two logit buffers from 384; P overwrites
-// the other logit buffer once that buffer's logits have been read.
+//   warps 12-15 softmax stage A: thread h owns head h (TMEM lane h): reads its logits of
+//               a tile, scales them, hands this CTA's partial to stage B through shared
+//               memory and to the peer CTA through distributed shared memory; loads Q;
+//   warps 8-11  softmax stage B: adds the two partials, online softmax in base 2 with a
+//               lazily raised reference max (the output is rescaled only when the max
+//               grows by more than 2^8), writes P as bf16 into TMEM, and at the end of a
+//               row normalises O and writes it out (or merges split rows).
+// TMEM columns: O [0,256) | Q latent [256,384) | two logit buffers from 384.  P tiles are
+// double-buffered in shared memory, so a logit buffer is free again as soon as stage A has
+// read it.
 //
 // FP8 numerics.  Each CTA's 256 latent dims are two 128-blocks with their own scales
 // s_lo, s_hi, so the logit needs two accumulators: acc_lo = q_lo . k_lo and
@@ -64,16 +69,16 @@ struct TcCfg;
 // gather lands on a 128-B aligned stride.
 template <>
 struct TcCfg<DCP_KV_FP8_E4M3_S128> {
-  static constexpr int NACC = 2, NS = 4, NK = 3;
+  static constexpr int NACC = 2, NS = 3, NK = 3;
   static constexpr int LAT_TOK = 256, TAIL_TOK = 144, TAIL_GSTRIDE = 640;
 };
 template <>
 struct TcCfg<DCP_KV_BF16> {
-  static constexpr int NACC = 1, NS = 3, NK = 3;
+  static constexpr int NACC = 1, NS = 2, NK = 3;
   static constexpr int LAT_TOK = 512, TAIL_TOK = 64, TAIL_GSTRIDE = 256;
 };
 
-constexpr int kTcThreads = 384;
+constexpr int kTcThreads = 512;
 constexpr int kColO = 0, kColQ = 256, kColS = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kScaleFloor = 8.67361737988403547e-19f;  // 2^-60
@@ -96,8 +101,11 @@ struct TcLay {
   static constexpr int OFF_KT = 0;
   static constexpr int OFF_STG = OFF_KT + C::NK * KT_BYTES;
   static constexpr int OFF_QR = OFF_STG + C::NS * STG_BYTES;
-  static constexpr int OFF_X = OFF_QR + QR_BYTES;
-  static constexpr int OFF_META = OFF_X + 2 * X_BYTES;
+  static constexpr int P_BYTES = 128 * 128;   // P of a tile: 128 rows of one SW128 row
+  static constexpr int OFF_P = OFF_QR + QR_BYTES;
+  static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_SELF = OFF_X + 2 * X_BYTES;
+  static constexpr int OFF_META = OFF_SELF + 2 * X_BYTES;
   static constexpr int OFF_END = OFF_META + C::NK * META_BYTES;
   // at least 120 KB so that one CTA (and one TMEM owner) sits on an SM
   static constexpr int SMEM = (OFF_END + 1024 > 122880 ? OFF_END + 1024 : 122880);
@@ -108,8 +116,10 @@ struct TcLay {
 };
 
 struct TcShared {
-  uint64_t stg_full[4], stg_empty[4], kt_full[3], kt_empty[3];
+  uint64_t stg_full[4], stg_empty[4], kt_full[4], kt_empty[4];
   uint64_t s_full[2], p_full[2], pv_done[2], q_ready, in_full[2], out_free[2], drain;
+  uint64_t self_full[2], self_free[2];  // stage A -> stage B hand-over of this CTA's partial
+  uint64_t s_free[2];                   // stage A has read a logit buffer out of TMEM
   uint64_t fin_pub, fin_dec;  // split-unit publish / merge decision
   uint32_t stg_mask[4];
   uint32_t stg_issued[4];     // gathers issued per staging slot (for the teardown wait)
@@ -121,7 +131,7 @@ struct TcShared {
   int64_t unit0;
   int tile0, ntiles;
   int64_t scan_base;
-  int64_t warp_sum[12];
+  int64_t warp_sum[16];
 };
 
 struct UnitInfo {
@@ -205,8 +215,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
   constexpr int TN = kTN, NS = C::NS, NK = C::NK;
   constexpr bool FP8 = KVT == DCP_KV_FP8_E4M3_S128;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // 1024-B aligned base, derived from the shared array itself (keeps the address space)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ TcShared sh;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -238,6 +248,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       mbar_init(&sh.p_full[i], 4);
       mbar_init(&sh.in_full[i], 1);
       mbar_init(&sh.out_free[i], 4);  // one arrival per softmax warp of the peer
+      mbar_init(&sh.self_full[i], 4);
+      mbar_init(&sh.s_free[i], 4);
+      mbar_init(&sh.self_free[i], 4);
     }
     mbar_init(&sh.pv_done[0], 1);
     mbar_init(&sh.pv_done[1], 1);
@@ -308,13 +321,18 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
   const int ntiles = sh.ntiles;
   const int64_t T = sh.T, t0 = sh.t0;
 
-  if (warp >= 1 && warp <= 3) {
+  // Loader warps take tiles round-robin; a staging slot's empty barrier is waited on by
+  // parity, which tells phases apart only while the barrier is at most one phase behind:
+  // with NS >= NLD every loader's previous wait (tile j - NLD) has already seen tile
+  // j - NLD - NS >= j - 2 NS released.
+  constexpr int NLD = NS < 3 ? NS : 3;
+  static_assert(NS >= NLD, "staging slots must not be fewer than loader warps");
+  if (warp >= 1 && warp <= NLD) {
     // ============================================================ loaders
-    // Warp 1+li takes tiles j = li, li+3, ...; lane t handles slot t of a tile.  Stage I
+    // Warp 1+li takes tiles j = li, li+NLD, ...; lane t handles slot t of a tile.  Stage I
     // loads the tile's slot ids (two tiles of this warp ahead), stage T maps them to owner
     // shard / local slot and loads the block-table entry (one tile ahead), stage C turns
     // pages into pool rows and issues one latent and one tail gather per 4 slots.
-    constexpr int NLD = 3;
     const int li = warp - 1;
     if (li == 0 && lane == 0) {
       prefetch_tensormap(&tm_lat);
@@ -416,109 +434,120 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       t_has = n_has;
       t_x = n_x;
     }
+  } else if (warp >= 1 && warp <= 3) {
+    // a loader warp this configuration does not use
   } else if (warp == 0) {
     // ============================================================ MMA issuer
+    // Issues Q.K^T(jq) and P.V(jp) in whatever order their inputs become ready (P.V first:
+    // it frees a K slot and a P buffer), polling the barriers without blocking on either.
+    //   QK(jq): Q of its unit in TMEM (q_ready; the pair's first tile always loads Q), K tile
+    //           jq converted (kt_full), logit buffer jq&1 read by stage A(jq-2) (s_free);
+    //   PV(jp): P(jp) in shared memory (p_full).
     constexpr uint32_t idesc_qk = idesc_bf16(128, TN, 0, 0);
     constexpr uint32_t idesc_pv = FP8 ? idesc_bf16(128, 128, 0, 1) : idesc_bf16(128, 256, 0, 1);
     const uint32_t qb = tbase + kColQ;
     const uint64_t qrd = smem_desc(smem_u32(smem + L::OFF_QR), 16, 1024);
     const uint32_t leader = elect_one();
-    int q_phase = 0;
-    bool ok = true;
-    auto issue_qk = [&](int j, bool unit_first) -> bool {
-      if (unit_first) {
-        if (!mbar_wait(&sh.q_ready, q_phase & 1, abort_flag)) return false;
-        ++q_phase;
-      }
-      if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) return false;
-      // S buffer j&1 last held P(j-3) (P(m) is written into buffer (m+1)&1): its P.V must
-      // have read it -- the tensor pipe does not order that read before this write
-      if (j >= 3 && !mbar_wait(&sh.pv_done[(j - 3) & 1], ((j - 3) >> 1) & 1, abort_flag))
-        return false;
-      tc_fence_after();
-      {  // issued by one elected lane of the converged warp (operands stay warp-uniform)
-        const uint32_t kt = smem_u32(smem + L::OFF_KT + (j % NK) * L::KT_BYTES);
-        const uint32_t sb = tbase + kColS + (j & 1) * L::SBUF;
-        const uint64_t kd = smem_desc(kt, 16, 1024);
-        // start-address field (address >> 4) of K-step ks of the latent blocks / the RoPE block
-#define KOFF(ks) ((uint64_t)((((ks) >> 2) * L::BS + ((ks) & 3) * 32) >> 4))
-#define ROFF(i) ((uint64_t)((4 * L::BS + (i) * 32) >> 4))
-        if (FP8) {
-          // the two latent-block chains interleaved (consecutive MMAs write different
-          // accumulators), then the RoPE high parts and remainders into the lo chain
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int ks = (i >> 1) + 8 * (i & 1);
-            mma_ts_if(leader, sb + (i & 1) * TN, qb + 8 * ks, kd + KOFF(ks), idesc_qk,
-                      (ks & 7) != 0);
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            mma_ss_if(leader, sb, qrd + (uint64_t)(((i & 1) * 32) >> 4), kd + ROFF(i), idesc_qk, 1);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < 16; ++ks)
-            mma_ts_if(leader, sb, qb + 8 * ks, kd + KOFF(ks), idesc_qk, ks > 0);
-#pragma unroll
-          for (int i = 0; i < 2; ++i)
-            mma_ss_if(leader, sb, qrd + (uint64_t)((i * 32) >> 4), kd + ROFF(i), idesc_qk, 1);
-        }
-#undef KOFF
-#undef ROFF
-        mma_commit_if(leader, &sh.s_full[j & 1]);
-      }
-      return true;
-    };
-    // Q.K^T runs two tiles ahead of P.V: QK(j+2) overwrites S buffer j&1, which needs
-    // A(j) to have read S(j) (implied by p_full(j-1)) and P.V(j-1) to have read P(j-1)
-    // (waited for in issue_qk); for j = 0 the first condition is only known after p_full(0).
-    Walk<FUSED, SPARSE> w, wq;
-    w.init(p, sh.unit0, sh.tile0, ntiles);
-    wq = w;
-    // the softmax warps load Q for the pair's first unit even when it starts mid-unit
-    if (ntiles > 0) ok = issue_qk(0, true);
-    if (ok && ntiles > 1) {
-      wq.next(p);
-      ok = issue_qk(1, wq.first());
-    }
-    for (int j = 0; ok && j < ntiles; ++j) {
-      if (j >= 1 && j + 2 < ntiles) {
-        wq.next(p);
-        if (!(ok = issue_qk(j + 2, wq.first()))) break;
-      }
-      if (!(ok = mbar_wait(&sh.p_full[j & 1], (j >> 1) & 1, abort_flag))) break;
-      tc_fence_after();
-      {
-        const uint32_t kt = smem_u32(smem + L::OFF_KT + (j % NK) * L::KT_BYTES);
-        const uint32_t sb = tbase + kColS + ((j + 1) & 1) * L::SBUF;  // P(j)
+    Walk<FUSED, SPARSE> wq, wp;
+    wq.init(p, sh.unit0, sh.tile0, ntiles);
+    wp = wq;
+    int jq = 0, jp = 0, q_phase = 0;
+    uint64_t t_last = globaltimer();
+    int idle = 0;
+    while (jp < ntiles) {
+      bool progressed = false;
+      if (jp < jq && mbar_test(&sh.p_full[jp & 1], (jp >> 1) & 1)) {
+        tc_fence_after();
+        const uint32_t kt = smem_u32(smem + L::OFF_KT + (jp % NK) * L::KT_BYTES);
+        const uint64_t pd = smem_desc(smem_u32(smem + L::OFF_P + (jp & 1) * L::P_BYTES), 16, 1024);
         // a unit's (or this pair's) first tile overwrites O
-        const uint32_t acc0 = (w.first() || j == 0) ? 0u : 1u;
-        if (FP8) {  // P_lo = cols [0,16) (slots 0-15, 16-31), P_hi = cols [16,32)
-          mma_ts_if(leader, tbase + kColO, sb, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
-          mma_ts_if(leader, tbase + kColO + 128, sb + 16, smem_desc(kt + 2 * L::BS, L::BS, 1024),
-                    idesc_pv, acc0);
-          mma_ts_if(leader, tbase + kColO, sb + 8, smem_desc(kt + 2048, L::BS, 1024), idesc_pv, 1);
-          mma_ts_if(leader, tbase + kColO + 128, sb + 24,
+        const uint32_t acc0 = (wp.first() || jp == 0) ? 0u : 1u;
+        if (FP8) {  // P row: [p*s_lo for slots 0-31 | p*s_hi for slots 0-31]
+          mma_ss_if(leader, tbase + kColO, pd, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
+          mma_ss_if(leader, tbase + kColO + 128, pd + (64 >> 4),
+                    smem_desc(kt + 2 * L::BS, L::BS, 1024), idesc_pv, acc0);
+          mma_ss_if(leader, tbase + kColO, pd + (32 >> 4), smem_desc(kt + 2048, L::BS, 1024),
+                    idesc_pv, 1);
+          mma_ss_if(leader, tbase + kColO + 128, pd + (96 >> 4),
                     smem_desc(kt + 2 * L::BS + 2048, L::BS, 1024), idesc_pv, 1);
         } else {
-          mma_ts_if(leader, tbase + kColO, sb, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
-          mma_ts_if(leader, tbase + kColO, sb + 8, smem_desc(kt + 2048, L::BS, 1024), idesc_pv, 1);
+          mma_ss_if(leader, tbase + kColO, pd, smem_desc(kt, L::BS, 1024), idesc_pv, acc0);
+          mma_ss_if(leader, tbase + kColO, pd + (32 >> 4), smem_desc(kt + 2048, L::BS, 1024),
+                    idesc_pv, 1);
         }
-        mma_commit_if(leader, &sh.kt_empty[j % NK]);
-        mma_commit_if(leader, &sh.pv_done[j & 1]);
+        mma_commit_if(leader, &sh.kt_empty[jp % NK]);
+        mma_commit_if(leader, &sh.pv_done[jp & 1]);
+        wp.next(p);
+        ++jp;
+        progressed = true;
       }
-      if (j == 0 && 2 < ntiles) {
-        wq.next(p);
-        if (!(ok = issue_qk(2, wq.first()))) break;
+      if (jq < ntiles) {
+        const bool unit_first = jq == 0 || wq.first();
+        if ((!unit_first || mbar_test(&sh.q_ready, q_phase & 1)) &&
+            mbar_test(&sh.kt_full[jq % NK], (jq / NK) & 1) &&
+            (jq < 2 || mbar_test(&sh.s_free[jq & 1], ((jq - 2) >> 1) & 1))) {
+          if (unit_first) ++q_phase;
+          tc_fence_after();
+          const uint32_t kt = smem_u32(smem + L::OFF_KT + (jq % NK) * L::KT_BYTES);
+          const uint32_t sb = tbase + kColS + (jq & 1) * L::SBUF;
+          const uint64_t kd = smem_desc(kt, 16, 1024);
+          // start-address field (address >> 4) of K-step ks of the latent blocks / RoPE block
+#define KOFF(ks) ((uint64_t)((((ks) >> 2) * L::BS + ((ks) & 3) * 32) >> 4))
+#define ROFF(i) ((uint64_t)((4 * L::BS + (i) * 32) >> 4))
+          if (FP8) {
+            // the two latent-block chains interleaved (consecutive MMAs write different
+            // accumulators), then the RoPE high parts and remainders into the lo chain
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int ks = (i >> 1) + 8 * (i & 1);
+              mma_ts_if(leader, sb + (i & 1) * TN, qb + 8 * ks, kd + KOFF(ks), idesc_qk,
+                        (ks & 7) != 0);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mma_ss_if(leader, sb, qrd + (uint64_t)(((i & 1) * 32) >> 4), kd + ROFF(i), idesc_qk, 1);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 16; ++ks)
+              mma_ts_if(leader, sb, qb + 8 * ks, kd + KOFF(ks), idesc_qk, ks > 0);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              mma_ss_if(leader, sb, qrd + (uint64_t)((i * 32) >> 4), kd + ROFF(i), idesc_qk, 1);
+          }
+#undef KOFF
+#undef ROFF
+          mma_commit_if(leader, &sh.s_full[jq & 1]);
+          ++jq;
+          wq.next(p);
+          progressed = true;
+        }
       }
-      w.next(p);
+      if (progressed) {
+        idle = 0;
+        t_last = globaltimer();
+      } else {
+        if (*abort_flag) break;
+        if (++idle >= 32) {
+          idle = 0;
+          if (globaltimer() - t_last > kWaitLimitNs) {
+            *abort_flag = 1;
+            break;
+          }
+        }
+        __nanosleep(32);
+      }
     }
     mma_commit_elect(&sh.drain);
     volatile int no_abort = 0;
     mbar_wait(&sh.drain, 0, &no_abort);  // no MMA in flight before TMEM is released
   } else if (warp >= 4 && warp < 8) {
     // ============================================================ converters
+    // Latent part: thread -> slot t = 8*(warp-4) + 2*(lane>>3) + ((lane>>2)&1), 16-B chunks
+    // ch = (lane&3) + 4*(it ^ ((lane>>2)&1)): each 8-lane phase of a 16-B access reads 8
+    // distinct bank groups of the staging rows and writes 8 distinct swizzled chunks.
     const int ct = tid - 128;
+    const int l8 = lane & 7, hb = l8 >> 2;
+    const int t = 8 * (ct >> 5) + 2 * (lane >> 3) + hb;
     const float sl2 = p.scale_log2;
     for (int j = 0; j < ntiles; ++j) {
       const int slot = j % NS, ks = j % NK;
@@ -529,20 +558,24 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       unsigned char* kt = smem + L::OFF_KT + ks * L::KT_BYTES;
       unsigned char* meta = smem + L::OFF_META + ks * L::META_BYTES;
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      const bool live = (mask >> t) & 1;
       if (FP8) {
+        uint4 v[4];
 #pragma unroll
-        for (int it = 0; it < TN * 16 / 128; ++it) {  // 16 codes per item
-          const int q = ct + 128 * it;
-          const int t = q >> 4, ch = q & 15;
-          const uint4 v = (mask >> t) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + t * C::LAT_TOK + ch * 16)
-                              : zero;
-          const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        for (int it = 0; it < 4; ++it) {  // 16 codes per chunk
+          const int ch = (l8 & 3) + 4 * (it ^ hb);
+          v[it] = live ? *reinterpret_cast<const uint4*>(stg + t * C::LAT_TOK + ch * 16) : zero;
+        }
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int ch = (l8 & 3) + 4 * (it ^ hb);
+          const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
           uint32_t o[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            o[2 * e] = e4m3x2_to_bf16x2((uint16_t)(in[e] & 0xffffu));
-            o[2 * e + 1] = e4m3x2_to_bf16x2((uint16_t)(in[e] >> 16));
+            const uint2 w = e4m3x4_to_bf16x4(in[e]);
+            o[2 * e] = w.x;
+            o[2 * e + 1] = w.y;
           }
           unsigned char* base = kt + (ch >> 2) * L::BS + t * 128;
           const int c16 = (ch & 3) * 2;
@@ -550,12 +583,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           *reinterpret_cast<uint4*>(base + (((c16 + 1) ^ (t & 7)) << 4)) =
               make_uint4(o[4], o[5], o[6], o[7]);
         }
-        {  // RoPE: thread -> (slot t, 8 of this CTA's 32 dims); scales
-          const int t = ct >> 2, c4 = ct & 3;
-          const unsigned char* tail = stg + L::STG_TAIL + (t >> 2) * C::TAIL_GSTRIDE + (t & 3) * C::TAIL_TOK;
+        {  // RoPE: thread -> (slot rt, 8 of this CTA's 32 dims); scales
+          const int rt = ct >> 2, c4 = ct & 3;
+          const unsigned char* tail = stg + L::STG_TAIL + (rt >> 2) * C::TAIL_GSTRIDE + (rt & 3) * C::TAIL_TOK;
           uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
           float slo = 0.f, shi = 0.f, sf = 1.f;
-          if ((mask >> t) & 1) {
+          if ((mask >> rt) & 1) {
             const float4 sc = *reinterpret_cast<const float4*>(tail);
             slo = crank == 0 ? sc.x : sc.z;
             shi = crank == 0 ? sc.y : sc.w;
@@ -572,34 +605,36 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
               lw[e] = pack_bf16x2(y0 - __low2float(h2), y1 - __high2float(h2));
             }
           }
-          unsigned char* rb = kt + 4 * L::BS + t * 128;
-          *reinterpret_cast<uint4*>(rb + ((c4 ^ (t & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(rb + (((4 + c4) ^ (t & 7)) << 4)) =
+          unsigned char* rb = kt + 4 * L::BS + rt * 128;
+          *reinterpret_cast<uint4*>(rb + ((c4 ^ (rt & 7)) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(rb + (((4 + c4) ^ (rt & 7)) << 4)) =
               make_uint4(lw[0], lw[1], lw[2], lw[3]);
           if (c4 == 0) {
             float* mf = reinterpret_cast<float*>(meta + 16);
-            mf[t] = sf * sl2;
-            mf[TN + t] = shi * sl2;
-            mf[2 * TN + t] = slo;
-            mf[3 * TN + t] = shi;
+            mf[rt] = sf * sl2;
+            mf[TN + rt] = shi * sl2;
+            mf[2 * TN + rt] = slo;
+            mf[3 * TN + rt] = shi;
           }
         }
       } else {
+        uint4 v[8];
 #pragma unroll
-        for (int it = 0; it < TN * 32 / 128; ++it) {  // 8 bf16 per item
-          const int q = ct + 128 * it;
-          const int t = q >> 5, ch = q & 31;
-          const uint4 v = (mask >> t) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + t * C::LAT_TOK + ch * 16)
-                              : zero;
-          *reinterpret_cast<uint4*>(kt + (ch >> 3) * L::BS + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = v;
+        for (int it = 0; it < 8; ++it) {  // 8 bf16 per chunk
+          const int ch = (l8 & 3) + 4 * (it ^ hb);
+          v[it] = live ? *reinterpret_cast<const uint4*>(stg + t * C::LAT_TOK + ch * 16) : zero;
+        }
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int ch = (l8 & 3) + 4 * (it ^ hb);
+          *reinterpret_cast<uint4*>(kt + (ch >> 3) * L::BS + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = v[it];
         }
         {
-          const int t = ct >> 2, c4 = ct & 3;
-          const uint4 v = (mask >> t) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + L::STG_TAIL + t * C::TAIL_TOK + c4 * 16)
+          const int rt = ct >> 2, c4 = ct & 3;
+          const uint4 r = (mask >> rt) & 1
+                              ? *reinterpret_cast<const uint4*>(stg + L::STG_TAIL + rt * C::TAIL_TOK + c4 * 16)
                               : zero;
-          *reinterpret_cast<uint4*>(kt + 4 * L::BS + t * 128 + ((c4 ^ (t & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(kt + 4 * L::BS + rt * 128 + ((c4 ^ (rt & 7)) << 4)) = r;
         }
       }
       if (ct == 0) *reinterpret_cast<uint32_t*>(meta) = mask;
@@ -610,31 +645,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         mbar_arrive(&sh.stg_empty[slot]);
       }
     }
-  } else if (warp >= 8) {
-    // ============================================================ softmax / epilogue
-    const int h = tid - 256;  // head = TMEM lane
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t trow = tbase + lane_off;
-    const float sl2 = p.scale_log2;
+  } else if (warp >= 12) {
+    // ============================================================ softmax stage A
+    const int h = tid - 384;  // head = TMEM lane
+    const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     float* xin = reinterpret_cast<float*>(smem + L::OFF_X);
-
-    // units without any slot: zero output, -inf LSE
-    if (!(FUSED && SPARSE)) {
-      for (int64_t u = pair; u < U; u += P) {
-        const UnitInfo x = get_unit<FUSED, SPARSE>(p, u);
-        if (x.ntile != 0 || h >= H) continue;
-        const int64_t oi = (u * H + h) * kDv + crank * 256;
-        if (FUSED) {
-          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi);
-          for (int i = 0; i < 32; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi);
-          for (int i = 0; i < 64; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (crank == 0) p.lse[u * H + h] = -INFINITY;
-      }
-    }
-
+    float* xself = reinterpret_cast<float*>(smem + L::OFF_SELF);
     // Q of row r: this CTA's 256 latent dims into TMEM (two bf16 per column), its 32 RoPE
     // dims into row h of the SW128 A-operand tile in shared memory
     auto load_q = [&](int64_t r) {
@@ -664,9 +680,99 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       if (lane == 0) mbar_arrive(&sh.q_ready);
     };
 
+    Walk<FUSED, SPARSE> wa;
+    wa.init(p, sh.unit0, sh.tile0, ntiles);
+    // the pair's first unit, even when it starts mid-unit
+    if (ntiles > 0) load_q(wa.info.r);
+    for (int j = 0; j < ntiles; ++j) {
+      const int buf = j & 1;
+      if (!mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag)) break;
+      if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) break;
+      tc_fence_after();
+      const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
+      const uint32_t sb = trow + kColS + buf * L::SBUF;
+      float s[TN];
+      if (!FP8) {
+        uint32_t a[TN];
+        tmem_ld16(sb, a);
+        tmem_ld16(sb + 16, a + 16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * p.scale_log2;
+      } else {
+        const float4* ma = reinterpret_cast<const float4*>(meta + 16);
+        const float4* mb = ma + TN / 4;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t lo[16], hi[16];
+          tmem_ld16(sb + 16 * hf, lo);
+          tmem_ld16(sb + TN + 16 * hf, hi);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t4 = 0; t4 < 4; ++t4) {
+            const float4 a = ma[4 * hf + t4], b = mb[4 * hf + t4];
+            const int t = 16 * hf + 4 * t4;
+            s[t] = fmaf(__uint_as_float(lo[4 * t4]), a.x, __uint_as_float(hi[4 * t4]) * b.x);
+            s[t + 1] = fmaf(__uint_as_float(lo[4 * t4 + 1]), a.y, __uint_as_float(hi[4 * t4 + 1]) * b.y);
+            s[t + 2] = fmaf(__uint_as_float(lo[4 * t4 + 2]), a.z, __uint_as_float(hi[4 * t4 + 2]) * b.z);
+            s[t + 3] = fmaf(__uint_as_float(lo[4 * t4 + 3]), a.w, __uint_as_float(hi[4 * t4 + 3]) * b.w);
+          }
+        }
+      }
+      // logit buffer j&1 may take S(j+2) now
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.s_free[buf]);
+      // the next unit's queries go in once this tile's Q.K^T is done
+      if (wa.last() && j + 1 < ntiles) {
+        Walk<FUSED, SPARSE> wn = wa;
+        wn.next(p);
+        load_q(wn.info.r);
+      }
+      // this CTA's partial: to stage B through the local box (free once B(j-2) read it) ...
+      const int x = buf;
+      if (!mbar_wait(&sh.self_free[x], ((j >> 1) & 1) ^ 1, abort_flag)) break;
+      float* srow = xself + (x * 128 + h) * L::XSTRIDE;
+#pragma unroll
+      for (int c = 0; c < TN / 4; ++c)
+        *reinterpret_cast<float4*>(srow + 4 * c) = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.self_full[x]);
+      // ... and to the peer's inbox
+      if (!mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true)) break;
+      float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
+#pragma unroll
+      for (int c = 0; c < TN / 4; ++c)
+        st_async_v4(xrow + 4 * c, peer, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
+                    __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]), &sh.in_full[x]);
+      wa.next(p);
+    }
+  } else if (warp >= 8) {
+    // ============================================================ softmax stage B / epilogue
+    const int h = tid - 256;  // head = TMEM lane
+    const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    const float* xin = reinterpret_cast<const float*>(smem + L::OFF_X);
+    const float* xself = reinterpret_cast<const float*>(smem + L::OFF_SELF);
+
+    // units without any slot: zero output, -inf LSE
+    if (!(FUSED && SPARSE)) {
+      for (int64_t u = pair; u < U; u += P) {
+        const UnitInfo x = get_unit<FUSED, SPARSE>(p, u);
+        if (x.ntile != 0 || h >= H) continue;
+        const int64_t oi = (u * H + h) * kDv + crank * 256;
+        if (FUSED) {
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi);
+          for (int i = 0; i < 32; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi);
+          for (int i = 0; i < 64; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (crank == 0) p.lse[u * H + h] = -INFINITY;
+      }
+    }
+
     Walk<FUSED, SPARSE> w;
     w.init(p, sh.unit0, sh.tile0, ntiles);
-    if (ntiles > 0) load_q(w.info.r);
     float m_ref = -INFINITY, lsum = 0.f;
     int64_t U0 = t0 - sh.tile0;   // global index of the current unit's first tile
     bool from_start = sh.tile0 == 0;
@@ -792,79 +898,27 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       if (crank == 0 && h < H) p.lse[u * H + h] = mx == -INFINITY ? -INFINITY : mx + __log2f(W) * kLn2;
     };
 
-    // Stage A(j): read tile j's logits from TMEM, form this CTA's partial, send it to the
-    // peer.  Stage B(j): add the peer's partial, online softmax, P into TMEM, finish the
-    // unit.  Order A(0), A(1), B(0), A(2), B(1), ...: tile j's exchange is in flight while
-    // A(j+1) runs, so the DSMEM round trip leaves the critical path.
-    auto stage_a = [&](int j, const Walk<FUSED, SPARSE>& wa, float (&s)[TN]) -> bool {
-      const int buf = j & 1;
-      if (!mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag)) return false;
-      if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) return false;
-      tc_fence_after();
-      const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
-      const uint32_t sb = trow + kColS + buf * L::SBUF;
-      if (!FP8) {
-        uint32_t a[TN];
-        tmem_ld16(sb, a);
-        tmem_ld16(sb + 16, a + 16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * sl2;
-      } else {
-        const float4* ma = reinterpret_cast<const float4*>(meta + 16);
-        const float4* mb = ma + TN / 4;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t lo[16], hi[16];
-          tmem_ld16(sb + 16 * hf, lo);
-          tmem_ld16(sb + TN + 16 * hf, hi);
-          tmem_ld_wait();
-#pragma unroll
-          for (int t4 = 0; t4 < 4; ++t4) {
-            const float4 a = ma[4 * hf + t4], b = mb[4 * hf + t4];
-            const int t = 16 * hf + 4 * t4;
-            s[t] = fmaf(__uint_as_float(lo[4 * t4]), a.x, __uint_as_float(hi[4 * t4]) * b.x);
-            s[t + 1] = fmaf(__uint_as_float(lo[4 * t4 + 1]), a.y, __uint_as_float(hi[4 * t4 + 1]) * b.y);
-            s[t + 2] = fmaf(__uint_as_float(lo[4 * t4 + 2]), a.z, __uint_as_float(hi[4 * t4 + 2]) * b.z);
-            s[t + 3] = fmaf(__uint_as_float(lo[4 * t4 + 3]), a.w, __uint_as_float(hi[4 * t4 + 3]) * b.w);
-          }
-        }
-      }
-      // the next unit's queries go in once this tile's Q.K^T is done
-      if (wa.last() && j + 1 < ntiles) {
-        Walk<FUSED, SPARSE> wn = wa;
-        wn.next(p);
-        load_q(wn.info.r);
-      }
-      const int x = j & 1;
-      if (!mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true)) return false;
-      float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
-#pragma unroll
-      for (int c = 0; c < TN / 4; ++c)
-        st_async_v4(xrow + 4 * c, peer, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
-                    __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]), &sh.in_full[x]);
-      return true;
-    };
-
-    float s_cur[TN], s_nxt[TN];
     int j = 0;
-    if (ntiles > 0) ok = stage_a(0, w, s_cur);
     for (; ok && j < ntiles; ++j) {
-      if (j + 1 < ntiles) {
-        Walk<FUSED, SPARSE> wn = w;
-        wn.next(p);
-        if (!(ok = stage_a(j + 1, wn, s_nxt))) break;
-      }
-      // ---- stage B(j)
-      const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
-      const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
-      // P(j) goes into S buffer (j+1)&1: A(j+1) has already read S(j+1) out of it, and
-      // P(j-2), which it held before, has been read by P.V(j-2) (waited for below)
-      const uint32_t sb = trow + kColS + ((j + 1) & 1) * L::SBUF;
-      float s[TN];
-#pragma unroll
-      for (int t = 0; t < TN; ++t) s[t] = s_cur[t];
       const int x = j & 1;
+      const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
+      // P(j) goes into shared-memory buffer j&1 once P.V(j-2) has read P(j-2) (waited below)
+      unsigned char* prow = smem + L::OFF_P + (j & 1) * L::P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
+      float s[TN];
+      // A(j) hands over after it saw the K tile complete: the tile's metadata is valid
+      if (!(ok = mbar_wait(&sh.self_full[x], (j >> 1) & 1, abort_flag))) break;
+      const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
+      const float* srow = xself + (x * 128 + h) * L::XSTRIDE;
+#pragma unroll
+      for (int c = 0; c < TN / 4; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(srow + 4 * c);
+        s[4 * c] = v.x;
+        s[4 * c + 1] = v.y;
+        s[4 * c + 2] = v.z;
+        s[4 * c + 3] = v.w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.self_free[x]);
       if (!(ok = mbar_wait(&sh.in_full[x], (j >> 1) & 1, abort_flag, true))) break;
       const float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
 #pragma unroll
@@ -879,11 +933,21 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       // hands its rows back to the peer at the end of this stage
       if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&sh.in_full[x], 128 * TN * 4);
       // online softmax (base 2) with a lazily raised reference
-      float mt = -INFINITY;
+      if (mask != 0xffffffffu) {
 #pragma unroll
-      for (int t = 0; t < TN; ++t) {
-        if (!((mask >> t) & 1)) s[t] = -INFINITY;
-        mt = fmaxf(mt, s[t]);
+        for (int t = 0; t < TN; ++t)
+          if (!((mask >> t) & 1)) s[t] = -INFINITY;
+      }
+      float mt;
+      {
+        float r[TN / 2];
+#pragma unroll
+        for (int t = 0; t < TN / 2; ++t) r[t] = fmaxf(s[t], s[t + TN / 2]);
+#pragma unroll
+        for (int w2 = TN / 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int t = 0; t < w2; ++t) r[t] = fmaxf(r[t], r[t + w2]);
+        mt = r[0];
       }
       // per head: raise the reference when the tile max exceeds it by more than 2^8; the
       // TMEM read-modify-write of O is warp-collective, so a warp rescales when any of its
@@ -908,18 +972,29 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         m_ref = mt;
       }
       float pr[TN];
+      {
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;  // all -inf: every p is 0
 #pragma unroll
-      for (int t = 0; t < TN; ++t) {
-        pr[t] = m_ref == -INFINITY ? 0.f : fast_exp2(s[t] - m_ref);
-        lsum += pr[t];
+        for (int t = 0; t < TN; ++t) pr[t] = fast_exp2(s[t] - mr);
+        float r[TN / 2];
+#pragma unroll
+        for (int t = 0; t < TN / 2; ++t) r[t] = pr[t] + pr[t + TN / 2];
+#pragma unroll
+        for (int w2 = TN / 4; w2 >= 1; w2 >>= 1)
+#pragma unroll
+          for (int t = 0; t < w2; ++t) r[t] += r[t + w2];
+        lsum += r[0];
       }
       if (j >= 2 && !(ok = mbar_wait(&sh.pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag))) break;
-      tc_fence_after();
+      const int sw = h & 7;  // SW128: 16-B chunk c of row h sits at chunk c ^ (h & 7)
       if (!FP8) {
         uint32_t pw[TN / 2];
 #pragma unroll
         for (int i = 0; i < TN / 2; ++i) pw[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
-        tmem_st16(sb, pw);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
+              make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       } else {
         const float4* pl4 = reinterpret_cast<const float4*>(meta + 16 + 8 * TN);
         const float4* ph4 = pl4 + TN / 4;
@@ -932,10 +1007,16 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           phi[2 * i] = pack_bf16x2(pr[4 * i] * b.x, pr[4 * i + 1] * b.y);
           phi[2 * i + 1] = pack_bf16x2(pr[4 * i + 2] * b.z, pr[4 * i + 3] * b.w);
         }
-        tmem_st16(sb, plo);
-        tmem_st16(sb + TN / 2, phi);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
+              make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
+          *reinterpret_cast<uint4*>(prow + (((4 + c) ^ sw) << 4)) =
+              make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
+        }
       }
-      tmem_st_wait();
+      fence_proxy_async_smem();  // P is read by the tensor pipe
+      tmem_st_wait();            // (an O rescale above must land before P.V(j) accumulates)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -951,8 +1032,6 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         slot_idx = 1;
         U0 = t0 + j + 1;
       }
-#pragma unroll
-      for (int t = 0; t < TN; ++t) s_cur[t] = s_nxt[t];
       w.next(p);
     }
     // the range ended inside a unit (Walk.next does not move past the last tile):

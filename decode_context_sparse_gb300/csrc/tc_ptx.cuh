@@ -64,20 +64,35 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint64_t* bar, uint3
       "r"(rank)
       : "memory");
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps until it
+// completes or the hint (ns) runs out, instead of returning at once to spin.
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking test of a phase (never suspends): for issuers that poll several barriers.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
@@ -338,14 +353,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint16_t codes) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
   return ((h2 >> 3) & 0x0FFF0FFFu) | (h2 & 0x80008000u);
 }
-// Two E4M3 codes -> two bf16 of the same values, exactly: the image above times 2^112 (a
-// power-of-two product that neither rounds nor leaves the normal range: |v| <= 448,
-// smallest non-zero 2^-9).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t codes) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(e4m3x2_to_bf16x2_scaled(codes)), "r"(0x77807780u));
+// Four E4M3 codes (the bytes of x, lowest first) -> four bf16 of the same values, exactly,
+// two per word (lower code in the lower half), with integer operations only.  Each code's
+// four exponent and three mantissa bits are placed in the bf16 exponent field (low four
+// bits) and the top of its mantissa, the sign bit on the sign: a bf16 of value * 2^-120 for
+// every code (E4M3 subnormals, exponent 0, become bf16 subnormals with the same factor),
+// which a power-of-two product then brings back exactly.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t x) {
+  const uint32_t a = __byte_perm(x, 0u, 0x4140);  // code 0 | code 1 << 16
+  const uint32_t b = __byte_perm(x, 0u, 0x4342);  // code 2 | code 3 << 16
+  const uint32_t ia = ((a & 0x007F007Fu) << 4) | ((a & 0x00800080u) << 8);
+  const uint32_t ib = ((b & 0x007F007Fu) << 4) | ((b & 0x00800080u) << 8);
+  uint2 r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(ia), "r"(0x7B807B80u));  // * 2^120
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(ib), "r"(0x7B807B80u));
   return r;
 }
+
 
 }  // namespace tc
 }  // namespace dcp

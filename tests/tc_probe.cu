@@ -3,9 +3,10 @@
 //   mode 0: A in TMEM, B K-major (B given as [N][K] row-major)   -- the Q.K^T form
 //   mode 1: A in TMEM, B MN-major (B given as [K][N] row-major)  -- the P.V form
 //   mode 2: A in shared memory K-major, B K-major
+//   mode 3: A in shared memory K-major, B MN-major                -- the P.V form, P in smem
 // and a conversion probe for the exact E4M3 -> bf16 (x 2^-112) path.
-// Shapes accepted by tc_probe: K in {64, 128} (modes 0, 2) or {16, 32, 64, 128} (mode 1),
-// N a multiple of 16 in [16, 256] (modes 0, 2) or of 64 in [64, 256] (mode 1).
+// Shapes accepted by tc_probe: K in {64, 128} (modes 0, 2) or {16, 32, 64, 128} (modes 1, 3),
+// N a multiple of 16 in [16, 256] (modes 0, 2) or of 64 in [64, 256] (modes 1, 3).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,7 +38,8 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(const uint16_t* __restric
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (mode == 1) {  // [N/64 groups][K rows][128 B], swizzled
+  const bool b_mn = mode == 1 || mode == 3, a_smem = mode == 2 || mode == 3;
+  if (b_mn) {  // [N/64 groups][K rows][128 B], swizzled
     for (int i = tid; i < K * (N / 8); i += 128) {
       const int k = i / (N / 8), c8 = i % (N / 8), blk = c8 / 8, c = c8 % 8;
       const uint4 v = *reinterpret_cast<const uint4*>(B + (size_t)k * N + c8 * 8);
@@ -50,7 +52,7 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(const uint16_t* __restric
       *reinterpret_cast<uint4*>(sB + blk * (N * 128) + n * 128 + ((c ^ (n & 7)) * 16)) = v;
     }
   }
-  if (mode == 2) {  // A: [K/64 groups][128 rows][128 B], swizzled
+  if (a_smem) {  // A: [K/64 groups][128 rows][128 B], swizzled (K < 64: part of each row)
     for (int i = tid; i < 128 * (K / 8); i += 128) {
       const int m = i / (K / 8), c8 = i % (K / 8), blk = c8 / 8, c = c8 % 8;
       const uint4 v = *reinterpret_cast<const uint4*>(A + (size_t)m * K + c8 * 8);
@@ -63,7 +65,7 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(const uint16_t* __restric
   tc_fence_after();
   const uint32_t tbase = tmem_base;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  if (mode != 2) {  // row tid of A into TMEM columns [0, K/2)
+  if (!a_smem) {  // row tid of A into TMEM columns [0, K/2)
     const uint32_t* arow = reinterpret_cast<const uint32_t*>(A + (size_t)tid * K);
     for (int c = 0; c < K / 2; c += 8) {
       uint32_t r[8];
@@ -78,14 +80,14 @@ __global__ void __launch_bounds__(128) tc_probe_kernel(const uint16_t* __restric
   tc_fence_after();
   if (tid == 0) {
     const uint32_t d_tmem = tbase + 256;
-    const uint32_t idesc = idesc_bf16(128, N, 0, mode == 1 ? 1 : 0);
+    const uint32_t idesc = idesc_bf16(128, N, 0, b_mn ? 1 : 0);
     for (int ks = 0; ks < K / 16; ++ks) {
       uint64_t bdesc;
-      if (mode == 1)
+      if (b_mn)
         bdesc = smem_desc(smem_u32(sB) + ks * 2048, K * 128, 1024);
       else
         bdesc = smem_desc(smem_u32(sB) + (ks / 4) * (N * 128) + (ks % 4) * 32, 16, 1024);
-      if (mode == 2) {
+      if (a_smem) {
         const uint64_t adesc = smem_desc(smem_u32(sA) + (ks / 4) * (128 * 128) + (ks % 4) * 32, 16, 1024);
         mma_ss(d_tmem, adesc, bdesc, idesc, ks > 0);
       } else {
@@ -118,9 +120,20 @@ __global__ void e4m3_probe_kernel(const uint16_t* codes, uint32_t* out, int n) {
   if (i < n) out[i] = e4m3x2_to_bf16x2_scaled(codes[i]);
 }
 
+__global__ void e4m3x4_probe_kernel(const uint32_t* words, uint2* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = e4m3x4_to_bf16x4(words[i]);
+}
+
+extern "C" int e4m3x4_probe(const void* words, void* out, int n) {
+  e4m3x4_probe_kernel<<<(n + 255) / 256, 256>>>(static_cast<const uint32_t*>(words),
+                                                 static_cast<uint2*>(out), n);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
 extern "C" int tc_probe(const void* A, const void* B, float* D, int K, int N, int mode, int* err) {
   const bool kmaj = mode == 0 || mode == 2;
-  if (mode < 0 || mode > 2) return -1;
+  if (mode < 0 || mode > 3) return -1;
   if (kmaj && !(K == 64 || K == 128)) return -1;
   if (!kmaj && !(K == 16 || K == 32 || K == 64 || K == 128)) return -1;
   if (kmaj && (N < 16 || N > 256 || N % 16)) return -1;

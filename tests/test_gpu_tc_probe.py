@@ -24,6 +24,7 @@ def probe():
     lib = ctypes.CDLL(SO)
     lib.tc_probe.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     lib.e4m3_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.e4m3x4_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     return lib
 
 
@@ -38,11 +39,12 @@ def _run(lib, A, B, K, N, mode):
 
 @pytest.mark.parametrize("mode,K,N", [(0, 64, 16), (0, 64, 32), (0, 128, 64), (0, 128, 256),
                                       (2, 64, 16), (2, 128, 128),
-                                      (1, 16, 128), (1, 32, 64), (1, 32, 256), (1, 128, 256)])
+                                      (1, 16, 128), (1, 32, 64), (1, 32, 256), (1, 128, 256),
+                                      (3, 32, 128), (3, 32, 256), (3, 64, 128), (3, 64, 256)])
 def test_mma_layouts(probe, mode, K, N):
     g = torch.Generator(device="cuda").manual_seed(K * 1000 + N + mode)
     A = torch.randn((128, K), generator=g, device="cuda").to(torch.bfloat16)
-    if mode == 1:
+    if mode in (1, 3):
         B = torch.randn((K, N), generator=g, device="cuda").to(torch.bfloat16)
         ref = A.float() @ B.float()
     else:
@@ -60,5 +62,21 @@ def test_e4m3_to_bf16_exact(probe):
     got = out.view(torch.bfloat16).float().view(65536, 2).double() * 2.0 ** 112
     b = codes.view(torch.uint8).view(65536, 2)
     ref = b.view(torch.float8_e4m3fn).double()
+    finite = ~torch.isnan(ref)
+    assert torch.equal(got[finite], ref[finite])
+
+
+def test_e4m3x4_to_bf16_exact(probe):
+    """The integer E4M3 -> bf16 decode of the FP8 converter: every code in each byte
+    position (bytes 0-1 take all 65536 pairs, bytes 2-3 two other sweeps), compared with
+    torch's E4M3 decoding; the values must be identical (NaN codes excepted)."""
+    i = torch.arange(65536, dtype=torch.int64)
+    words = (i & 0xFF) | (((i >> 8) & 0xFF) << 8) | (((i * 37) & 0xFF) << 16) | (((i * 101 + 7) & 0xFF) << 24)
+    words = words.to(torch.int32).to("cuda")
+    out = torch.empty(65536, 2, dtype=torch.int32, device="cuda")
+    assert probe.e4m3x4_probe(words.data_ptr(), out.data_ptr(), 65536) == 0
+    torch.cuda.synchronize()
+    got = out.view(torch.bfloat16).float().view(65536, 4).double()
+    ref = words.view(torch.uint8).view(65536, 4).view(torch.float8_e4m3fn).double()
     finite = ~torch.isnan(ref)
     assert torch.equal(got[finite], ref[finite])
