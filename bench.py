@@ -116,6 +116,9 @@ def dist_env():
     return ws, rank, local
 
 
+TRAFFIC_BYTES_PER_ROW = (181.371392e6 + 18.441472e6) / 96
+
+
 def make_workload(dev, seqs=64):
     import synth
     return synth.cfg3_sparse_topk2048_fp8(device=dev, seqs=seqs)
@@ -334,14 +337,17 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": hbm_tbs * 1e3, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_tbs * 1e3 / peaks["hbm_gbs"]}
-    roof["traffic"] = None
+    # DRAM bytes (read + write) per launch from ncu (profiles/decode_tc_fused_topk2048_fp8_96rows.md:
+    # 181.4 MB + 18.4 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
+    roof["traffic"] = TRAFFIC_BYTES_PER_ROW * R if prob.heads == 128 else None
+    roof["traffic_unit"] = "bytes"
     roof["peak_src"] = peaks["src"]
     roof["kernel"] = "mla_decode_dcp_fused"
     roof["roofline_us"] = 1e6 * max(t_hbm, t_tc)
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": avg_ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": os.environ.get("DCP_BENCH_DTYPE", "f32"),
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "rows": R, "heads": prob.heads, "topk": prob.k,
                    "dcp": prob.dcp, "interleave": prob.interleave, "context": 131072,

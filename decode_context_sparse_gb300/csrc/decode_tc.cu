@@ -69,12 +69,12 @@ struct TcCfg;
 // gather lands on a 128-B aligned stride.
 template <>
 struct TcCfg<DCP_KV_FP8_E4M3_S128> {
-  static constexpr int NACC = 2, NS = 3, NK = 3;
+  static constexpr int NACC = 2, NS = 3, NK = 4;
   static constexpr int LAT_TOK = 256, TAIL_TOK = 144, TAIL_GSTRIDE = 640;
 };
 template <>
 struct TcCfg<DCP_KV_BF16> {
-  static constexpr int NACC = 1, NS = 2, NK = 3;
+  static constexpr int NACC = 1, NS = 2, NK = 4;
   static constexpr int LAT_TOK = 512, TAIL_TOK = 64, TAIL_GSTRIDE = 256;
 };
 
@@ -93,7 +93,9 @@ struct TcLay {
   static constexpr int STG_BYTES = STG_TAIL + (TN / 4) * C::TAIL_GSTRIDE;
   static constexpr int GROUP_TX = 4 * (C::LAT_TOK + C::TAIL_TOK);  // bytes of one 4-row group
   static constexpr int QR_BYTES = 128 * 128;  // RoPE part of Q: 128 rows of one SW128 row
-  static constexpr int XSTRIDE = TN + 4;      // floats per exchange row (16-B aligned rows)
+  // exchange rows: TN floats, 16-B chunk c of row h stored at chunk c ^ (h & 7) (a warp's
+  // accesses to one chunk of 32 rows then spread over all banks)
+  static constexpr int XSTRIDE = TN;
   static constexpr int X_BYTES = 128 * XSTRIDE * 4;
   // per K tile: mask | logit scale lo | logit scale hi | P scale lo | P scale hi
   static constexpr int META_BYTES = 16 + 4 * TN * 4;
@@ -105,7 +107,7 @@ struct TcLay {
   static constexpr int OFF_P = OFF_QR + QR_BYTES;
   static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
   static constexpr int OFF_SELF = OFF_X + 2 * X_BYTES;
-  static constexpr int OFF_META = OFF_SELF + 2 * X_BYTES;
+  static constexpr int OFF_META = OFF_SELF + X_BYTES;  // one local box
   static constexpr int OFF_END = OFF_META + C::NK * META_BYTES;
   // at least 120 KB so that one CTA (and one TMEM owner) sits on an SM
   static constexpr int SMEM = (OFF_END + 1024 > 122880 ? OFF_END + 1024 : 122880);
@@ -116,9 +118,9 @@ struct TcLay {
 };
 
 struct TcShared {
-  uint64_t stg_full[4], stg_empty[4], kt_full[4], kt_empty[4];
+  uint64_t stg_full[4], stg_empty[4], kt_full[8], kt_empty[8];
   uint64_t s_full[2], p_full[2], pv_done[2], q_ready, in_full[2], out_free[2], drain;
-  uint64_t self_full[2], self_free[2];  // stage A -> stage B hand-over of this CTA's partial
+  uint64_t self_full, self_free;        // stage A -> stage B hand-over of this CTA's partial
   uint64_t s_free[2];                   // stage A has read a logit buffer out of TMEM
   uint64_t fin_pub, fin_dec;  // split-unit publish / merge decision
   uint32_t stg_mask[4];
@@ -248,9 +250,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       mbar_init(&sh.p_full[i], 4);
       mbar_init(&sh.in_full[i], 1);
       mbar_init(&sh.out_free[i], 4);  // one arrival per softmax warp of the peer
-      mbar_init(&sh.self_full[i], 4);
       mbar_init(&sh.s_free[i], 4);
-      mbar_init(&sh.self_free[i], 4);
     }
     mbar_init(&sh.pv_done[0], 1);
     mbar_init(&sh.pv_done[1], 1);
@@ -258,6 +258,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     mbar_init(&sh.fin_dec, 1);
     mbar_init(&sh.q_ready, 4);
     mbar_init(&sh.drain, 1);
+    mbar_init(&sh.self_full, 4);
+    mbar_init(&sh.self_free, 4);
     sh.abort_flag = 0;
     fence_mbar_init();
     // the exchange inboxes expect one tile of partial logits each
@@ -729,21 +731,22 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         wn.next(p);
         load_q(wn.info.r);
       }
-      // this CTA's partial: to stage B through the local box (free once B(j-2) read it) ...
+      // this CTA's partial: to stage B through the local box (free once B(j-1) read it) ...
       const int x = buf;
-      if (!mbar_wait(&sh.self_free[x], ((j >> 1) & 1) ^ 1, abort_flag)) break;
-      float* srow = xself + (x * 128 + h) * L::XSTRIDE;
+      if (!mbar_wait(&sh.self_free, (j & 1) ^ 1, abort_flag)) break;
+      float* srow = xself + h * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c)
-        *reinterpret_cast<float4*>(srow + 4 * c) = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+        *reinterpret_cast<float4*>(srow + 4 * (c ^ (h & 7))) =
+            make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.self_full[x]);
+      if (lane == 0) mbar_arrive(&sh.self_full);
       // ... and to the peer's inbox
       if (!mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true)) break;
       float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c)
-        st_async_v4(xrow + 4 * c, peer, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
+        st_async_v4(xrow + 4 * (c ^ (h & 7)), peer, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
                     __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]), &sh.in_full[x]);
       wa.next(p);
     }
@@ -906,24 +909,24 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       unsigned char* prow = smem + L::OFF_P + (j & 1) * L::P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
       float s[TN];
       // A(j) hands over after it saw the K tile complete: the tile's metadata is valid
-      if (!(ok = mbar_wait(&sh.self_full[x], (j >> 1) & 1, abort_flag))) break;
+      if (!(ok = mbar_wait(&sh.self_full, j & 1, abort_flag))) break;
       const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
-      const float* srow = xself + (x * 128 + h) * L::XSTRIDE;
+      const float* srow = xself + h * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(srow + 4 * c);
+        const float4 v = *reinterpret_cast<const float4*>(srow + 4 * (c ^ (h & 7)));
         s[4 * c] = v.x;
         s[4 * c + 1] = v.y;
         s[4 * c + 2] = v.z;
         s[4 * c + 3] = v.w;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.self_free[x]);
+      if (lane == 0) mbar_arrive(&sh.self_free);
       if (!(ok = mbar_wait(&sh.in_full[x], (j >> 1) & 1, abort_flag, true))) break;
       const float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * c);
+        const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * (c ^ (h & 7)));
         s[4 * c] += v.x;
         s[4 * c + 1] += v.y;
         s[4 * c + 2] += v.z;
@@ -949,6 +952,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           for (int t = 0; t < w2; ++t) r[t] = fmaxf(r[t], r[t + w2]);
         mt = r[0];
       }
+      // every inbox value of this warp has been loaded and used (the max depends on all of
+      // them): hand the rows back to the peer now; a relaxed arrive suffices
+      asm volatile("" ::"f"(mt) : "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(&sh.out_free[x], peer);
       // per head: raise the reference when the tile max exceeds it by more than 2^8; the
       // TMEM read-modify-write of O is warp-collective, so a warp rescales when any of its
       // heads needs it (alpha = 1 for the others)
@@ -1019,11 +1027,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       tmem_st_wait();            // (an O rescale above must land before P.V(j) accumulates)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sh.p_full[j & 1]);
-        // this warp's inbox rows were read (and used) above: a relaxed arrive suffices
-        mbar_arrive_cluster_relaxed(&sh.out_free[x], peer);
-      }
+      if (lane == 0) mbar_arrive(&sh.p_full[j & 1]);
       if (w.last()) {
         finish_unit(j, from_start);
         m_ref = -INFINITY;
@@ -1105,7 +1109,8 @@ bool tc_path_enabled() {
 
 // The pool as a 2-D tensor [num_pages * 64 rows][row elements] for the 4-row gathers:
 // FP8 rows as 656 bytes (latent box 256 B, tail box 144 B from byte 512), BF16 rows as 576
-// bf16 (latent box 256 elements, RoPE box 32 elements).
+// bf16 (latent box 256 elements, RoPE box 32 elements).  No L2 promotion: rows are 656 /
+// 1152 B apart, so promoting a box to 256-B lines would fetch bytes no box asks for.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1138,11 +1143,11 @@ static cudaError_t make_pool_maps(const DecodeParams& p, int kv_dtype, CUtensorM
   const cuuint32_t es[2] = {1, 1};
   void* base = const_cast<uint8_t*>(p.pool);
   if (enc(lat, dt, 2, base, dims, strides, box_lat, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   if (enc(tail, dt, 2, base, dims, strides, box_tail, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   return cudaSuccess;
