@@ -69,12 +69,12 @@ struct TcCfg;
 // gather lands on a 128-B aligned stride.
 template <>
 struct TcCfg<DCP_KV_FP8_E4M3_S128> {
-  static constexpr int NACC = 2, NS = 3, NK = 4;
+  static constexpr int NACC = 2, NS = 3, NK = 4, NP = 2;
   static constexpr int LAT_TOK = 256, TAIL_TOK = 144, TAIL_GSTRIDE = 640;
 };
 template <>
 struct TcCfg<DCP_KV_BF16> {
-  static constexpr int NACC = 1, NS = 2, NK = 4;
+  static constexpr int NACC = 1, NS = 2, NK = 4, NP = 2;
   static constexpr int LAT_TOK = 512, TAIL_TOK = 64, TAIL_GSTRIDE = 256;
 };
 
@@ -98,23 +98,24 @@ struct TcLay {
   // unpadded layout for the remote st.async stores.
   static constexpr int XSTRIDE = TN + 4;
   static constexpr int X_BYTES = 128 * XSTRIDE * 4;
-  // per K tile: mask | logit scale lo | logit scale hi | P scale lo | P scale hi
-  static constexpr int META_BYTES = 16 + 4 * TN * 4;
+  // per K tile: logit scale lo | logit scale hi | P scale lo | P scale hi (the slot mask is
+  // kept in TcShared::kt_mask)
+  static constexpr int META_BYTES = 4 * TN * 4;
   static constexpr int SBUF = C::NACC * TN;
   static constexpr int OFF_KT = 0;
   static constexpr int OFF_STG = OFF_KT + C::NK * KT_BYTES;
   static constexpr int OFF_QR = OFF_STG + C::NS * STG_BYTES;
   static constexpr int P_BYTES = 128 * 128;   // P of a tile: 128 rows of one SW128 row
   static constexpr int OFF_P = OFF_QR + QR_BYTES;
-  static constexpr int OFF_X = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_X = OFF_P + C::NP * P_BYTES;
   static constexpr int OFF_SELF = OFF_X + 2 * X_BYTES;
-  static constexpr int OFF_META = OFF_SELF + X_BYTES;  // one local box
+  static constexpr int SELF_BYTES = X_BYTES;  // the local box: same padded rows
+  static constexpr int OFF_META = OFF_SELF + SELF_BYTES;
   static constexpr int OFF_END = OFF_META + C::NK * META_BYTES;
   // at least 120 KB so that one CTA (and one TMEM owner) sits on an SM
   static constexpr int SMEM = (OFF_END + 1024 > 122880 ? OFF_END + 1024 : 122880);
   static_assert(OFF_STG % 1024 == 0 && STG_BYTES % 1024 == 0 && OFF_QR % 1024 == 0,
                 "SW128 tiles and TMA destinations need 1024-B / 128-B alignment");
-  static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(kColS + 2 * SBUF <= (int)kTmemCols, "TMEM columns");
 };
 
@@ -125,6 +126,7 @@ struct TcShared {
   uint64_t s_free[2];                   // stage A has read a logit buffer out of TMEM
   uint64_t fin_pub, fin_dec;  // split-unit publish / merge decision
   uint32_t stg_mask[4];
+  uint32_t kt_mask[8];        // valid-slot mask of each K tile
   uint32_t stg_issued[4];     // gathers issued per staging slot (for the teardown wait)
   uint32_t tmem_base;
   int abort_flag;
@@ -134,8 +136,10 @@ struct TcShared {
   int64_t unit0;
   int tile0, ntiles;
   int64_t scan_base;
-  int64_t warp_sum[16];
 };
+// dynamic + static shared memory within the 227 KB a CTA may opt into
+static_assert(TcLay<DCP_KV_FP8_E4M3_S128>::SMEM + sizeof(TcShared) <= 232448, "shared memory");
+static_assert(TcLay<DCP_KV_BF16>::SMEM + sizeof(TcShared) <= 232448, "shared memory");
 
 struct UnitInfo {
   int64_t r;
@@ -184,7 +188,8 @@ struct Walk {
 };
 
 // Block-wide exclusive prefix of v (384 threads); returns the prefix, *total the sum.
-__device__ __forceinline__ int64_t block_scan_excl(int64_t v, TcShared& sh, int64_t* total) {
+// (warp_sum: 16 int64 of shared memory, free during set-up)
+__device__ __forceinline__ int64_t block_scan_excl(int64_t v, int64_t* warp_sum, int64_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int64_t x = v;
 #pragma unroll
@@ -192,12 +197,12 @@ __device__ __forceinline__ int64_t block_scan_excl(int64_t v, TcShared& sh, int6
     const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) sh.warp_sum[warp] = x;
+  if (lane == 31) warp_sum[warp] = x;
   __syncthreads();
   int64_t base = 0, tot = 0;
   for (int w = 0; w < kTcThreads / 32; ++w) {
-    if (w < warp) base += sh.warp_sum[w];
-    tot += sh.warp_sum[w];
+    if (w < warp) base += warp_sum[w];
+    tot += warp_sum[w];
   }
   __syncthreads();
   *total = tot;
@@ -269,6 +274,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
   }
 
   // this pair's contiguous range of the tile sequence
+  int64_t* scan_tmp = reinterpret_cast<int64_t*>(smem + L::OFF_META);  // metadata is unused yet
   if (FUSED && SPARSE) {
     const int64_t tu = (p.k + TN - 1) / TN;
     const int64_t T = U * tu;
@@ -286,7 +292,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     int64_t part = 0;
     for (int64_t u = tid; u < U; u += kTcThreads) part += get_unit<FUSED, SPARSE>(p, u).ntile;
     int64_t T;
-    block_scan_excl(part, sh, &T);
+    block_scan_excl(part, scan_tmp, &T);
     const int Pe = (int)(T < P ? (T > 0 ? T : 1) : P);
     const int64_t t0 = pair < Pe ? pair * T / Pe : T, t1 = pair < Pe ? (pair + 1) * T / Pe : T;
     if (tid == 0) {
@@ -304,7 +310,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         const int64_t u = c0 + tid;
         const int nt = u < U ? get_unit<FUSED, SPARSE>(p, u).ntile : 0;
         int64_t chunk_total;
-        const int64_t excl = block_scan_excl(nt, sh, &chunk_total) + sh.scan_base;
+        const int64_t excl = block_scan_excl(nt, scan_tmp, &chunk_total) + sh.scan_base;
         if (nt > 0 && t0 >= excl && t0 < excl + nt) {
           sh.unit0 = u;
           sh.tile0 = (int)(t0 - excl);
@@ -462,7 +468,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       if (jp < jq && mbar_test(&sh.p_full[jp & 1], (jp >> 1) & 1)) {
         tc_fence_after();
         const uint32_t kt = smem_u32(smem + L::OFF_KT + (jp % NK) * L::KT_BYTES);
-        const uint64_t pd = smem_desc(smem_u32(smem + L::OFF_P + (jp & 1) * L::P_BYTES), 16, 1024);
+        const uint64_t pd = smem_desc(smem_u32(smem + L::OFF_P + (jp % C::NP) * L::P_BYTES), 16, 1024);
         // a unit's (or this pair's) first tile overwrites O
         const uint32_t acc0 = (wp.first() || jp == 0) ? 0u : 1u;
         if (FP8) {  // P row: [p*s_lo for slots 0-31 | p*s_hi for slots 0-31]
@@ -613,7 +619,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           *reinterpret_cast<uint4*>(rb + (((4 + c4) ^ (rt & 7)) << 4)) =
               make_uint4(lw[0], lw[1], lw[2], lw[3]);
           if (c4 == 0) {
-            float* mf = reinterpret_cast<float*>(meta + 16);
+            float* mf = reinterpret_cast<float*>(meta);
             mf[rt] = sf * sl2;
             mf[TN + rt] = shi * sl2;
             mf[2 * TN + rt] = slo;
@@ -640,7 +646,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           *reinterpret_cast<uint4*>(kt + 4 * L::BS + rt * 128 + ((c4 ^ (rt & 7)) << 4)) = r;
         }
       }
-      if (ct == 0) *reinterpret_cast<uint32_t*>(meta) = mask;
+      if (ct == 0) sh.kt_mask[ks] = mask;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {  // one arrival per warp (arrivals of 128 threads serialise)
@@ -703,7 +709,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
 #pragma unroll
         for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * p.scale_log2;
       } else {
-        const float4* ma = reinterpret_cast<const float4*>(meta + 16);
+        const float4* ma = reinterpret_cast<const float4*>(meta);
         const float4* mb = ma + TN / 4;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -906,12 +912,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     for (; ok && j < ntiles; ++j) {
       const int x = j & 1;
       const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
-      // P(j) goes into shared-memory buffer j&1 once P.V(j-2) has read P(j-2) (waited below)
-      unsigned char* prow = smem + L::OFF_P + (j & 1) * L::P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
+      // P(j) goes into shared-memory buffer j % NP once P.V(j-NP) has read it (waited below)
+      unsigned char* prow = smem + L::OFF_P + (j % C::NP) * L::P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
       float s[TN];
       // A(j) hands over after it saw the K tile complete: the tile's metadata is valid
       if (!(ok = mbar_wait(&sh.self_full, j & 1, abort_flag))) break;
-      const uint32_t mask = *reinterpret_cast<const uint32_t*>(meta);
+      const uint32_t mask = sh.kt_mask[j % NK];
       const float* srow = xself + h * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c) {
@@ -994,7 +1000,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           for (int t = 0; t < w2; ++t) r[t] += r[t + w2];
         lsum += r[0];
       }
-      if (j >= 2 && !(ok = mbar_wait(&sh.pv_done[j & 1], ((j - 2) >> 1) & 1, abort_flag))) break;
+      if (j >= C::NP &&
+          !(ok = mbar_wait(&sh.pv_done[(j - C::NP) & 1], ((j - C::NP) >> 1) & 1, abort_flag)))
+        break;
       const int sw = h & 7;  // SW128: 16-B chunk c of row h sits at chunk c ^ (h & 7)
       if (!FP8) {
         uint32_t pw[TN / 2];
@@ -1005,7 +1013,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
               make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       } else {
-        const float4* pl4 = reinterpret_cast<const float4*>(meta + 16 + 8 * TN);
+        const float4* pl4 = reinterpret_cast<const float4*>(meta + 8 * TN);
         const float4* ph4 = pl4 + TN / 4;
         uint32_t plo[TN / 2], phi[TN / 2];
 #pragma unroll

@@ -358,12 +358,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint16_t codes) {
 // four exponent and three mantissa bits are placed in the bf16 exponent field (low four
 // bits) and the top of its mantissa, the sign bit on the sign: a bf16 of value * 2^-120 for
 // every code (E4M3 subnormals, exponent 0, become bf16 subnormals with the same factor),
-// which a power-of-two product then brings back exactly.
+// which a power-of-two product then brings back exactly.  The byte permute replicates each
+// code's sign over the byte above it (selector nibbles with bit 3 set), so one shift and one
+// mask place both codes of a word half.
 __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t x) {
-  const uint32_t a = __byte_perm(x, 0u, 0x4140);  // code 0 | code 1 << 16
-  const uint32_t b = __byte_perm(x, 0u, 0x4342);  // code 2 | code 3 << 16
-  const uint32_t ia = ((a & 0x007F007Fu) << 4) | ((a & 0x00800080u) << 8);
-  const uint32_t ib = ((b & 0x007F007Fu) << 4) | ((b & 0x00800080u) << 8);
+  uint32_t a, b;  // [code, sign x 8, code, sign x 8] for codes 0,1 and 2,3
+  asm("prmt.b32 %0, %1, 0, 0x9180;" : "=r"(a) : "r"(x));
+  asm("prmt.b32 %0, %1, 0, 0xB3A2;" : "=r"(b) : "r"(x));
+  const uint32_t ia = (a << 4) & 0x87F087F0u;
+  const uint32_t ib = (b << 4) & 0x87F087F0u;
   uint2 r;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.x) : "r"(ia), "r"(0x7B807B80u));  // * 2^120
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r.y) : "r"(ib), "r"(0x7B807B80u));
