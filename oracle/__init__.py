@@ -80,6 +80,13 @@ def _load():
         lib.orc_merge.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
         lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_e4m3_encode.restype = ctypes.c_int
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_kv_write.restype = ctypes.c_int64
+        lib.orc_kv_write.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                     ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                     ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
         _lib = lib
     return _lib
 
@@ -213,3 +220,26 @@ def merge(part_out, part_lse):
     if rc != 0:
         raise RuntimeError("oracle merge failed: %d" % rc)
     return out, lse
+
+
+def e4m3_encode(y: float) -> int:
+    """Nearest E4M3 code of the fp32 value y (ties to even, saturating at 448)."""
+    return _load().orc_e4m3_encode(float(y))
+
+
+def kv_write(kv, seq, pos, pool, kv_dtype: int, block_table, dcp: int, interleave: int,
+             shard: int = -1):
+    """DCP KV-cache write of token rows kv [n, 576] (bf16) at (seq[i], pos[i]) into a copy of
+    pool [num_pages, page_size, token_bytes]; returns (new pool uint8, written, skipped)."""
+    kvb = _np(kv, np.uint8).reshape(-1, 1152)
+    n = kvb.shape[0]
+    seq_a = _np(seq, np.int32).reshape(-1)
+    pos_a = _np(pos, np.int32).reshape(-1)
+    out = _np(pool, np.uint8).copy()
+    num_pages, page_size = out.shape[0], out.shape[1]
+    bt = _np(block_table, np.int32)
+    skipped = ctypes.c_int64(0)
+    written = _load().orc_kv_write(_ptr(kvb), n, _ptr(seq_a), _ptr(pos_a), int(dcp), int(interleave),
+                                   int(shard), _ptr(out), num_pages, int(kv_dtype), page_size,
+                                   _ptr(bt), bt.shape[1], bt.shape[2], ctypes.byref(skipped))
+    return out, int(written), int(skipped.value)

@@ -258,3 +258,99 @@ int orc_merge(const double* part_out, const double* part_lse, int32_t dcp, int64
   }
   return 0;
 }
+
+/* ---- KV-cache write (interleaved DCP) -----------------------------------------------
+ * A new token's latent row (576 bf16: 512 latent, 64 RoPE) at global position t of
+ * sequence b is stored on shard s = owner(t) at that shard's local slot l = local(t):
+ * page block_table[s][b][l / page_size], row l mod page_size (LMDeploy PR #4952, files:
+ * "Interleaved DCP KV-cache writes").  FP8 pools quantise the latent part and keep the RoPE
+ * part in bf16 (SGLang PR #36990, review of quantize_k_cache_separate: the "nope" and "pe"
+ * parts are quantised separately).  Per block of 128 latent values: scale = amax / 448 in
+ * fp32 (0 for an all-zero block, whose codes are 0), code = the E4M3 value nearest to
+ * value / scale computed in fp32, ties to the even code, saturating at 448.  The code
+ * decision is taken in fp32, the precision the writer computes in. */
+
+/* Nearest E4M3 code of y (round to nearest, ties to even, saturate to +-448), by search
+ * over the 127 non-negative finite codes. */
+int orc_e4m3_encode(float y) {
+  if (y != y) return 0x7F;
+  const int sign = signbit(y) ? 1 : 0;
+  double a = fabs((double)y);
+  if (a > 448.0) a = 448.0;
+  int best = 0;
+  double bestd = INFINITY;
+  for (int c = 0; c < 127; ++c) {
+    const double d = fabs(orc_e4m3_decode(c) - a);
+    if (d < bestd || (d == bestd && (c & 1) == 0)) {
+      best = c;
+      bestd = d;
+    }
+  }
+  return best | (sign << 7);
+}
+
+static float bf16_bits_to_float(const uint8_t* p) {
+  uint16_t h;
+  memcpy(&h, p, 2);
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* Writes n token rows kv[n][576] (bf16 bytes) of sequences seq[i] at global positions
+ * pos[i] into the pool; shard >= 0 writes only the rows that shard owns.  Rows whose
+ * position or sequence is negative / out of range, or whose block-table entry is missing or
+ * out of range, are skipped and counted in *skipped.  Returns the number of rows written. */
+int64_t orc_kv_write(const uint8_t* kv, int64_t n, const int32_t* seq, const int32_t* pos,
+                     int32_t dcp, int32_t interleave, int32_t shard, uint8_t* pool,
+                     int64_t num_pages, int32_t kv_dtype, int32_t page_size,
+                     const int32_t* block_table, int32_t num_seqs, int32_t bt_stride,
+                     int64_t* skipped) {
+  const int tb = kv_dtype == ORC_KV_BF16 ? 1152 : 656;
+  int64_t written = 0, skip = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t t = pos[i];
+    const int b = seq[i];
+    if (t < 0 || b < 0 || b >= num_seqs) {
+      ++skip;
+      continue;
+    }
+    const int s = orc_owner(t, dcp, interleave);
+    if (shard >= 0 && s != shard) continue;
+    const int64_t l = orc_local(t, dcp, interleave);
+    const int64_t pj = l / page_size;
+    if (pj >= bt_stride) {
+      ++skip;
+      continue;
+    }
+    const int32_t page = block_table[((int64_t)s * num_seqs + b) * bt_stride + pj];
+    if (page < 0 || page >= num_pages) {
+      ++skip;
+      continue;
+    }
+    uint8_t* dst = pool + ((int64_t)page * page_size + l % page_size) * tb;
+    const uint8_t* src = kv + i * (int64_t)(ORC_DQK * 2);
+    if (kv_dtype == ORC_KV_BF16) {
+      memcpy(dst, src, 1152);
+    } else {
+      for (int blk = 0; blk < 4; ++blk) {
+        float amax = 0.0f;
+        for (int j = 0; j < 128; ++j) {
+          const float v = fabsf(bf16_bits_to_float(src + 2 * (blk * 128 + j)));
+          if (v > amax) amax = v;
+        }
+        const float scale = amax / 448.0f;
+        for (int j = 0; j < 128; ++j) {
+          const float v = bf16_bits_to_float(src + 2 * (blk * 128 + j));
+          dst[blk * 128 + j] = (uint8_t)(scale > 0.0f ? orc_e4m3_encode(v / scale) : 0);
+        }
+        memcpy(dst + 512 + 4 * blk, &scale, 4);
+      }
+      memcpy(dst + 528, src + 1024, 128);
+    }
+    ++written;
+  }
+  if (skipped) *skipped = skip;
+  return written;
+}
