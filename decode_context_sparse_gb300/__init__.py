@@ -35,7 +35,7 @@ TOKEN_BYTES = {DCP_KV_BF16: 1152, DCP_KV_FP8_E4M3_S128: 656}
 # every symbol include/dcpmla.h declares
 EXPORTS = ("dcp_status_string", "dcp_abi_version", "dcp_remap_topk", "dcp_local_lengths",
            "mla_decode_partial_lse", "dcp_lse_merge", "mla_decode_dcp_fused",
-           "mla_decode_workspace_size", "mla_decode_dcp_fused_noalloc")
+           "mla_decode_workspace_size", "mla_decode_dcp_fused_noalloc", "dcp_kv_cache_write")
 DCP_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -92,6 +92,9 @@ def load(path: str = LIB_PATH):
     lib.mla_decode_dcp_fused.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32, V]
     lib.mla_decode_dcp_fused_noalloc.restype = ctypes.c_int
     lib.mla_decode_dcp_fused_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32, V]
+    lib.dcp_kv_cache_write.restype = ctypes.c_int
+    lib.dcp_kv_cache_write.argtypes = [V, I64, V, V, I32, I32, I32, V, I64, I32, I32, V, I32, I32,
+                                       I32, V, V]
     lib.mla_decode_workspace_size.restype = SZ
     lib.mla_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32]
     if lib.dcp_abi_version() != DCP_ABI_VERSION:
@@ -162,6 +165,29 @@ def dcp_local_lengths(global_len: torch.Tensor, dcp: int, interleave: int, shard
     _check(load().dcp_local_lengths(_ptr(global_len), rows, dcp, interleave, shard,
                                     _ptr(local_len), _stream(stream)), "dcp_local_lengths")
     return local_len
+
+
+# ------------------------------------------------------------------------------ cache write
+def dcp_kv_cache_write(kv: torch.Tensor, seq: torch.Tensor, pos: torch.Tensor, kv_pool: torch.Tensor,
+                       kv_dtype: int, block_table: torch.Tensor, dcp: int, interleave: int,
+                       shard: int = -1, checked: bool = False, err_flag: Optional[torch.Tensor] = None,
+                       stream=None):
+    """Write token rows kv [n, 576] bf16 at (seq, pos) into kv_pool [pages, 64, bytes] (in
+    place) on their owner shard; FP8 pools are quantised per 128 latent values."""
+    if kv.dtype != torch.bfloat16 or kv.dim() != 2 or kv.shape[1] != 576:
+        raise ValueError("kv must be [n, 576] bf16")
+    _i32(seq, "seq")
+    _i32(pos, "pos")
+    _i32(block_table, "block_table")
+    n = kv.shape[0]
+    if seq.numel() != n or pos.numel() != n:
+        raise ValueError("seq and pos must have n entries")
+    num_pages, page_size = kv_pool.shape[0], kv_pool.shape[1]
+    _check(load().dcp_kv_cache_write(_ptr(kv), n, _ptr(seq), _ptr(pos), dcp, interleave, shard,
+                                     _ptr(kv_pool), num_pages, kv_dtype, page_size, _ptr(block_table),
+                                     block_table.shape[1], block_table.shape[2], 1 if checked else 0,
+                                     _ptr(err_flag), _stream(stream)), "dcp_kv_cache_write")
+    return kv_pool
 
 
 # ------------------------------------------------------------------------------ merge

@@ -149,6 +149,24 @@ int dcp_local_lengths(const int32_t* global_len, int64_t rows, int32_t dcp, int3
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int dcp_kv_cache_write(const void* kv, int64_t n, const int32_t* seq, const int32_t* pos,
+                       int32_t dcp, int32_t interleave, int32_t shard, void* kv_pool,
+                       int64_t num_pages, int32_t kv_dtype, int32_t page_size,
+                       const int32_t* block_table, int32_t num_seqs, int32_t bt_stride,
+                       int32_t checked, int32_t* err_flag, dcp_stream_t stream) {
+  if (!kv || !seq || !pos || !kv_pool || !block_table) return DCP_ERR_INVALID_ARG;
+  if (n < 0 || num_pages < 1 || num_seqs < 1 || bt_stride < 1) return DCP_ERR_INVALID_ARG;
+  if (!valid_rule(dcp, interleave) || shard < -1 || shard >= dcp) return DCP_ERR_INVALID_ARG;
+  if (!aligned(kv, 16) || !aligned(kv_pool, 16)) return DCP_ERR_INVALID_ARG;
+  if (kv_dtype != DCP_KV_BF16 && kv_dtype != DCP_KV_FP8_E4M3_S128) return DCP_ERR_UNSUPPORTED;
+  if (page_size != 64) return DCP_ERR_UNSUPPORTED;
+  if (n == 0) return DCP_OK;
+  return status_of(launch_kv_write(kv, n, seq, pos, dcp, interleave, shard, kv_pool, num_pages,
+                                   kv_dtype, block_table, num_seqs, bt_stride,
+                                   checked ? err_flag : nullptr,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int dcp_lse_merge(const float* part_out, const float* part_lse, int32_t dcp, int64_t rows,
                   int32_t heads, int32_t dv, void* out, float* lse, dcp_stream_t stream) {
   if (!part_out || !part_lse || !out || !lse) return DCP_ERR_INVALID_ARG;

@@ -48,6 +48,10 @@ cudaError_t launch_remap_topk(const int32_t* gidx, int64_t rows, int k, int D, i
                               int32_t* local_idx, int32_t* count, cudaStream_t st);
 cudaError_t launch_local_lengths(const int32_t* glen, int64_t rows, int D, int I, int shard,
                                  int32_t* llen, cudaStream_t st);
+cudaError_t launch_kv_write(const void* kv, int64_t n, const int32_t* seq, const int32_t* pos,
+                            int D, int I, int shard, void* pool, int64_t num_pages, int kv_dtype,
+                            const int32_t* bt, int num_seqs, int bt_stride, int32_t* err,
+                            cudaStream_t st);
 cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int D, int64_t rows,
                              int heads, int dv, void* out, float* lse, cudaStream_t st);
 

@@ -1,0 +1,114 @@
+// DCP KV-cache write: new token rows into the paged pool of their owner shard, FP8 pools
+// quantised per 128 latent values (LMDeploy PR #4952 "support decode context parallelism
+// for PyTorch MLA", files: "Interleaved DCP KV-cache writes"; SGLang PR #36990 "DCP for
+// DSA models with the flashmla_kv backend", review of quantize_k_cache_separate: the
+// latent and RoPE parts are quantised separately).
+//
+// One warp per token row.  FP8: lane l holds latent values [16l, 16l+16); the 8 lanes of a
+// 128-value block reduce its amax, scale = amax / 448 (IEEE fp32 division), every value is
+// divided by the scale (IEEE) and rounded to nearest-even E4M3 with saturation at 448 by the
+// hardware conversion; an all-zero block stores scale 0 and zero codes.  RoPE (64 bf16) is
+// copied.  BF16: the 1152-byte row is copied.  HBM-bound: 1152 B read and 656 / 1152 B
+// written per row.
+#include "common.cuh"
+#include "internal.h"
+
+namespace dcp {
+
+constexpr int kKvwThreads = 256;
+constexpr int kKvwRowsPerCta = kKvwThreads / 32;
+
+// Two fp32 -> two E4M3 codes (round to nearest even, saturating), lo in the low byte.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int KVT>
+__global__ void __launch_bounds__(kKvwThreads)
+kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restrict__ seq,
+                const int32_t* __restrict__ pos, int D, int I, int shard, uint8_t* pool,
+                int64_t num_pages, const int32_t* __restrict__ bt, int num_seqs, int bt_stride,
+                int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * kKvwRowsPerCta;
+  for (int64_t i = (int64_t)blockIdx.x * kKvwRowsPerCta + (threadIdx.x >> 5); i < n; i += stride) {
+    const int t = __ldg(pos + i), b = __ldg(seq + i);
+    if (t < 0) continue;  // padding
+    if (b < 0 || b >= num_seqs) {
+      if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
+      continue;
+    }
+    const int s = owner_of(t, D, I);
+    if (shard >= 0 && s != shard) continue;
+    const int l = local_of(t, D, I);
+    const int pj = l >> 6;  // page size 64
+    if (pj >= bt_stride) {
+      if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
+      continue;
+    }
+    const int page = __ldg(bt + ((int64_t)s * num_seqs + b) * bt_stride + pj);
+    if (page < 0 || page >= num_pages) {
+      if (lane == 0) set_err(err, DCP_ERRBIT_PAGE_RANGE);
+      continue;
+    }
+    const uint4* src = kv + i * (kDqk * 2 / 16);  // 72 chunks of 16 B
+    if (KVT == DCP_KV_BF16) {
+      uint4* dst = reinterpret_cast<uint4*>(pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesBF16);
+      for (int c = lane; c < 72; c += 32) dst[c] = __ldg(src + c);
+    } else {
+      uint8_t* row = pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesFP8;
+      const uint4 a = __ldg(src + 2 * lane), c = __ldg(src + 2 * lane + 1);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      float v[16];
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[2 * e] = bf16_lo(w[e]);
+        v[2 * e + 1] = bf16_hi(w[e]);
+        amax = fmaxf(amax, fmaxf(fabsf(v[2 * e]), fabsf(v[2 * e + 1])));
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float scale = amax / 448.0f;
+      uint32_t q[4] = {0u, 0u, 0u, 0u};
+      if (scale > 0.f) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          q[e] = f32x2_to_e4m3x2(v[4 * e] / scale, v[4 * e + 1] / scale) |
+                 (f32x2_to_e4m3x2(v[4 * e + 2] / scale, v[4 * e + 3] / scale) << 16);
+      }
+      *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
+      if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + 4 * (lane >> 3)) = scale;
+      if (lane < 8)
+        *reinterpret_cast<uint4*>(row + 528 + 16 * lane) = __ldg(src + 64 + lane);
+    }
+  }
+}
+
+cudaError_t launch_kv_write(const void* kv, int64_t n, const int32_t* seq, const int32_t* pos,
+                            int D, int I, int shard, void* pool, int64_t num_pages, int kv_dtype,
+                            const int32_t* bt, int num_seqs, int bt_stride, int32_t* err,
+                            cudaStream_t st) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 148;
+  }
+  const int64_t need = (n + kKvwRowsPerCta - 1) / kKvwRowsPerCta;
+  const int grid = (int)(need < (int64_t)sms * 16 ? need : (int64_t)sms * 16);
+  const uint4* k4 = static_cast<const uint4*>(kv);
+  uint8_t* p8 = static_cast<uint8_t*>(pool);
+  if (kv_dtype == DCP_KV_BF16)
+    kv_write_kernel<DCP_KV_BF16><<<grid, kKvwThreads, 0, st>>>(k4, n, seq, pos, D, I, shard, p8,
+                                                               num_pages, bt, num_seqs, bt_stride, err);
+  else
+    kv_write_kernel<DCP_KV_FP8_E4M3_S128><<<grid, kKvwThreads, 0, st>>>(
+        k4, n, seq, pos, D, I, shard, p8, num_pages, bt, num_seqs, bt_stride, err);
+  return cudaGetLastError();
+}
+
+}  // namespace dcp

@@ -106,6 +106,38 @@ int dcp_local_lengths(const int32_t* global_len, int64_t rows, int32_t dcp,
                       dcp_stream_t stream);
 
 /*
+ * dcp_kv_cache_write -- store new token rows in the paged pool of their owner shard.
+ * Passage: LMDeploy PR #4952, files: "Interleaved DCP KV-cache writes" (each new token is
+ *   written to the shard the owner rule assigns it, at that shard's local slot); SGLang
+ *   PR #36990, review of quantize_k_cache_separate (an FP8 cache quantises the latent
+ *   ("nope") part and keeps the RoPE part separately).
+ *
+ * kv         (device) [n][576] bf16 token rows (latent 0..511, RoPE 512..575), 16-B aligned.
+ * seq, pos   (device) [n] int32: sequence index and global position of each row; a negative
+ *            position is padding (skipped).
+ * dcp, interleave  the owner rule (see above); shard -1 writes every row, 0..D-1 only the
+ *            rows that shard owns.
+ * kv_pool    (device) [num_pages][page_size][token bytes], written in place, 16-B aligned.
+ * block_table (device) [dcp][num_seqs][bt_stride] int32, as for the fused decode: entry j of
+ *            (shard, sequence) is the page holding local slots j*64 .. j*64+63.
+ * FP8 rows: per block of 128 latent values scale = amax / 448 (fp32), codes = value / scale
+ *   (fp32) rounded to the nearest E4M3 value, ties to even, saturating at 448; an all-zero
+ *   block stores scale 0 and zero codes; RoPE is stored as given.  BF16 rows are copied.
+ *   The bytes written are identical to that definition (exact integer result).
+ * Rows whose sequence or block-table entry is out of range are skipped; with checked != 0
+ *   they set DCP_ERRBIT_SLOT_RANGE / DCP_ERRBIT_PAGE_RANGE in *err_flag.  Rows of one call
+ *   must not share a destination slot (the stored row is then unspecified).
+ * Errors: DCP_ERR_INVALID_ARG for null or misaligned pointers, n < 0, num_pages < 1,
+ *   num_seqs < 1, bt_stride < 1, a bad owner rule or shard; DCP_ERR_UNSUPPORTED for another
+ *   page size or kv_dtype.  n = 0 is a no-op.
+ */
+int dcp_kv_cache_write(const void* kv, int64_t n, const int32_t* seq, const int32_t* pos,
+                       int32_t dcp, int32_t interleave, int32_t shard, void* kv_pool,
+                       int64_t num_pages, int32_t kv_dtype, int32_t page_size,
+                       const int32_t* block_table, int32_t num_seqs, int32_t bt_stride,
+                       int32_t checked, int32_t* err_flag, dcp_stream_t stream);
+
+/*
  * Arguments of the decode entry points.  Field meaning differs between the per-shard
  * call (mla_decode_partial_lse) and the fused call (mla_decode_dcp_fused) where noted.
  */

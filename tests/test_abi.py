@@ -108,3 +108,27 @@ def test_decode_rejects_bad_arguments(lib):
     # (48..128 heads) always reserves its split-unit partials and tickets
     assert lib.mla_decode_workspace_size(R(_args(num_splits=1, heads=32)), 8, 1) == 0
     assert lib.mla_decode_workspace_size(R(_args(num_splits=1)), 8, 1) > 0
+
+
+def test_kv_cache_write_rejects_bad_arguments(lib):
+    import decode_context_sparse_gb300 as dcp
+    g = ctypes.c_void_p(1 << 20)
+    call = lib.dcp_kv_cache_write
+    ok = dict(kv=g, n=4, seq=g, pos=g, dcp=2, interleave=1, shard=-1, pool=g, num_pages=8,
+              kv_dtype=1, page_size=64, bt=g, num_seqs=1, bt_stride=4, checked=0, err=None)
+
+    def run(**kw):
+        a = dict(ok, **kw)
+        return call(a["kv"], a["n"], a["seq"], a["pos"], a["dcp"], a["interleave"], a["shard"],
+                    a["pool"], a["num_pages"], a["kv_dtype"], a["page_size"], a["bt"],
+                    a["num_seqs"], a["bt_stride"], a["checked"], a["err"], None)
+    assert run(kv=None) == dcp.DCP_ERR_INVALID_ARG
+    assert run(pool=None) == dcp.DCP_ERR_INVALID_ARG
+    assert run(kv=ctypes.c_void_p((1 << 20) + 8)) == dcp.DCP_ERR_INVALID_ARG   # misaligned rows
+    assert run(n=-1) == dcp.DCP_ERR_INVALID_ARG
+    assert run(dcp=0) == dcp.DCP_ERR_INVALID_ARG
+    assert run(shard=2) == dcp.DCP_ERR_INVALID_ARG
+    assert run(num_pages=0) == dcp.DCP_ERR_INVALID_ARG
+    assert run(page_size=32) == dcp.DCP_ERR_UNSUPPORTED
+    assert run(kv_dtype=3) == dcp.DCP_ERR_UNSUPPORTED
+    assert run(n=0) == dcp.DCP_OK    # nothing to do, nothing launched
