@@ -177,6 +177,40 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def time_kv_cache_write(dcp, dev, peaks, stream, flush, steps):
+    """The cache-fill call before the path: 64 sequences x 2048 new tokens written into an FP8
+    pool (D = 8, token-interleaved), timed like the decode (events, L2 flushed between
+    calls).  Algorithmic bytes per row: 1152 read + 8 (sequence, position) + 656 written."""
+    seqs, T, D = 64, 2048, 8
+    gen = torch.Generator(device=dev).manual_seed(7)
+    pages = D * seqs * (T // D // 64)
+    bt = torch.randperm(pages, device=dev, generator=gen).to(torch.int32).view(D, seqs, -1)
+    kv = torch.randn((seqs * T, 576), device=dev, generator=gen).to(torch.bfloat16)
+    seq = torch.arange(seqs, device=dev, dtype=torch.int32).repeat_interleave(T)
+    pos = torch.arange(T, device=dev, dtype=torch.int32).repeat(seqs)
+    pool = torch.zeros((pages, 64, 656), dtype=torch.uint8, device=dev)
+
+    def call():
+        dcp.dcp_kv_cache_write(kv, seq, pos, pool, 1, bt, D, 1)
+
+    for _ in range(3):
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(max(3, steps))]
+    for a, b in evs:
+        flush.fill_(3)
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    nbytes = seqs * T * (1152 + 8 + 656)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"rows": seqs * T, "kv_dtype": "fp8_e4m3_per128_scale", "dcp": D, "us": 1e3 * ms,
+            "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"],
+            "frac": gbs / peaks["hbm_gbs"], "bound": "hbm", "launches_per_call": 1}
+
+
 def cpu_baseline_sample(prob):
     """Oracle timed on host cores on a bounded sample of the same workload (rank 0, N = 1)."""
     import oracle
@@ -282,6 +316,7 @@ def main():
         b.record(stream)
     torch.cuda.synchronize()
     unfused_ms = statistics.mean(a.elapsed_time(b) for a, b in uev)
+    kvw = time_kv_cache_write(dcp, dev, peaks, stream, flush, args.steps)
 
     # end to end through the public API with host buffers: H2D of the step's inputs (queries,
     # top-k ids, row map, block tables) from pinned memory, D2H of the outputs
@@ -361,6 +396,7 @@ def main():
         "unfused": {"ms_per_step": unfused_ms, "rows_per_s": R / (unfused_ms / 1e3),
                     "launches_per_step": 3},
         "roofline": roof,
+        "kv_cache_write": kvw,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
