@@ -82,7 +82,7 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   p.use_tc = (tc_path_enabled() && a->heads > 32 && a->num_pages <= (int64_t)(INT32_MAX / 64)) ? 1 : 0;
   p.pairs = 0;
   p.tc_o = p.tc_l = nullptr;
-  p.tc_cnt = nullptr;
+  p.tc_desc = nullptr;
   p.err_timeout = a->err_flag;  // timeouts are reported whenever err_flag is given
   if (p.use_tc) {
     const int tn = tc_tile_slots(a->kv_dtype);
@@ -103,7 +103,7 @@ int bind_workspace(const dcp_mla_decode_args* a, DecodeParams& p, cudaStream_t s
     if (a->workspace == nullptr || a->workspace_bytes < need || !aligned(a->workspace, 256))
       return DCP_ERR_WORKSPACE;
     tc_bind_workspace(p, a->workspace);
-    return status_of(cudaMemsetAsync(p.tc_cnt, 0, tc_ticket_bytes(p.num_units), st));
+    return status_of(cudaMemsetAsync(p.tc_desc, 0, tc_clear_bytes(p.pairs), st));
   }
   const size_t need = simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
   if (need == 0) return DCP_OK;

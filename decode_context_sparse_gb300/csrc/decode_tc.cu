@@ -124,13 +124,11 @@ struct TcShared {
   uint64_t s_full[2], p_full[2], pv_done[2], q_ready, in_full[2], out_free[2], drain;
   uint64_t self_full, self_free;        // stage A -> stage B hand-over of this CTA's partial
   uint64_t s_free[2];                   // stage A has read a logit buffer out of TMEM
-  uint64_t fin_pub, fin_dec;  // split-unit publish / merge decision
   uint32_t stg_mask[4];
   uint32_t kt_mask[8];        // valid-slot mask of each K tile
   uint32_t stg_issued[4];     // gathers issued per staging slot (for the teardown wait)
   uint32_t tmem_base;
   int abort_flag;
-  int last_flag;
   int64_t T, t0;
   int Peff;  // pairs that own tiles: min(pairs, T), so no pair's range is empty
   int64_t unit0;
@@ -260,8 +258,6 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     }
     mbar_init(&sh.pv_done[0], 1);
     mbar_init(&sh.pv_done[1], 1);
-    mbar_init(&sh.fin_pub, 4);
-    mbar_init(&sh.fin_dec, 1);
     mbar_init(&sh.q_ready, 4);
     mbar_init(&sh.drain, 1);
     mbar_init(&sh.self_full, 4);
@@ -328,6 +324,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
   tc_fence_after();
   const uint32_t tbase = sh.tmem_base;
   const int ntiles = sh.ntiles;
+  if (blockIdx.x == 0 && tid == 0) {  // the tile sequence, for the split-merge kernel
+    p.tc_desc[0] = sh.T;
+    p.tc_desc[1] = sh.Peff;
+  }
   const int64_t T = sh.T, t0 = sh.t0;
 
   // Loader warps take tiles round-robin; a staging slot's empty barrier is waited on by
@@ -787,7 +787,6 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     int64_t U0 = t0 - sh.tile0;   // global index of the current unit's first tile
     bool from_start = sh.tile0 == 0;
     int slot_idx = 0;             // workspace slot of a split unit: 0 first unit, 1 last
-    int fin_phase = 0;
     bool ok = true;
 
     // Finish the current unit: normalise and write O (or a split partial) and the LSE.
@@ -833,79 +832,15 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         if (crank == 0 && h < H) p.lse[u * H + h] = lse_v;
         return;
       }
-      // split unit: publish, and merge if this pair finishes it last
+      // split unit: publish this pair's partial and its descriptor; the split-merge kernel
+      // that follows on the stream combines the parts of every split unit
       __stcg(p.tc_l + (((int64_t)pair * 2 + slot_idx) * 2 + crank) * 128 + h, lse_v);
-      __threadfence();
-      const int64_t U1 = U0 + w.info.ntile;
-      const int64_t Pe = sh.Peff;  // pair q starts at tile q*T/Pe
-      const int64_t pf = min(Pe - 1, ((U0 + 1) * Pe - 1) / T);
-      const int64_t pl = min(Pe - 1, (U1 * Pe - 1) / T);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.fin_pub);
-      if (warp == 8) {  // every thread of this CTA has published: take a ticket
-        if (lane == 0) {
-          sh.last_flag = 0;
-          if (mbar_wait(&sh.fin_pub, fin_phase & 1, abort_flag)) {
-            __threadfence();
-            const unsigned prev = atomicAdd(p.tc_cnt + u * 2 + crank, 1u);
-            sh.last_flag = prev == (unsigned)(pl - pf);
-          }
-          mbar_arrive(&sh.fin_dec);
-        }
-        __syncwarp();
+      if (crank == 0 && h == 0) {
+        int64_t* d = p.tc_desc + 2 + ((int64_t)pair * 2 + slot_idx) * 3;
+        d[0] = u;
+        d[1] = U0;
+        d[2] = U0 + w.info.ntile;
       }
-      const bool dec = mbar_wait(&sh.fin_dec, fin_phase & 1, abort_flag);
-      ++fin_phase;
-      if (!dec || !sh.last_flag) return;
-      __threadfence();
-      float mx = -INFINITY;
-      for (int64_t q = pf; q <= pl; ++q) {
-        const int sq = (q * T / Pe) >= U0 ? 0 : 1;
-        mx = fmaxf(mx, __ldcg(p.tc_l + ((q * 2 + sq) * 2 + crank) * 128 + h));
-      }
-      float W = 0.f;
-      float acc[16];
-      for (int c = 0; c < 16; ++c) {
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-        W = 0.f;
-        if (mx != -INFINITY) {
-          for (int64_t q = pf; q <= pl; ++q) {
-            const int sq = (q * T / Pe) >= U0 ? 0 : 1;
-            const float lq = __ldcg(p.tc_l + ((q * 2 + sq) * 2 + crank) * 128 + h);
-            const float wq = fast_exp2((lq - mx) * kLog2e);
-            W += wq;
-            if (wq == 0.f) continue;
-            const float4* src = reinterpret_cast<const float4*>(
-                p.tc_o + ((q * 2 + sq) * 128 + h) * kDv + crank * 256 + 16 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 v4 = __ldcg(src + i);
-              acc[4 * i] = fmaf(wq, v4.x, acc[4 * i]);
-              acc[4 * i + 1] = fmaf(wq, v4.y, acc[4 * i + 1]);
-              acc[4 * i + 2] = fmaf(wq, v4.z, acc[4 * i + 2]);
-              acc[4 * i + 3] = fmaf(wq, v4.w, acc[4 * i + 3]);
-            }
-          }
-        }
-        const float iw = W > 0.f ? 1.0f / W : 0.f;
-        if (h < H) {
-          if (FUSED) {
-            uint32_t b2[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) b2[i] = pack_bf16x2(acc[2 * i] * iw, acc[2 * i + 1] * iw);
-            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
-            o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
-            o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
-          } else {
-            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi + 16 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              o[i] = make_float4(acc[4 * i] * iw, acc[4 * i + 1] * iw, acc[4 * i + 2] * iw,
-                                 acc[4 * i + 3] * iw);
-          }
-        }
-      }
-      if (crank == 0 && h < H) p.lse[u * H + h] = mx == -INFINITY ? -INFINITY : mx + __log2f(W) * kLn2;
     };
 
     int j = 0;
@@ -1074,10 +1009,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
 // ------------------------------------------------------------------ host side
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+size_t tc_clear_bytes(int pairs);
+
 size_t tc_workspace_bytes(int64_t units, int pairs) {
+  (void)units;
   return a256((size_t)pairs * 2 * 128 * kDv * sizeof(float)) +
-         a256((size_t)pairs * 2 * 2 * 128 * sizeof(float)) +
-         a256((size_t)units * 2 * sizeof(unsigned));
+         a256((size_t)pairs * 2 * 2 * 128 * sizeof(float)) + a256(tc_clear_bytes(pairs));
 }
 
 void tc_bind_workspace(DecodeParams& p, void* ws) {
@@ -1086,10 +1023,79 @@ void tc_bind_workspace(DecodeParams& p, void* ws) {
   const size_t l = a256((size_t)p.pairs * 2 * 2 * 128 * sizeof(float));
   p.tc_o = reinterpret_cast<float*>(b);
   p.tc_l = reinterpret_cast<float*>(b + o);
-  p.tc_cnt = reinterpret_cast<unsigned*>(b + o + l);
+  p.tc_desc = reinterpret_cast<int64_t*>(b + o + l);
 }
 
-size_t tc_ticket_bytes(int64_t units) { return (size_t)units * 2 * sizeof(unsigned); }
+// Tile-sequence header (T, pairs owning tiles) and one descriptor (unit, first tile, end
+// tile) per (pair, slot), cleared before every call.
+size_t tc_clear_bytes(int pairs) { return (2 + (size_t)pairs * 2 * 3) * sizeof(int64_t); }
+
+// Merges the parts of units that several pairs' ranges cut.  One CTA per (descriptor,
+// CTA half, 16-column chunk) and one thread per head: a descriptor is merged by its pair
+// when that pair is the unit's first covering pair (exactly one per split unit).  Part q
+// holds the unit in workspace slot 0 when its range starts inside the unit, else in slot 1.
+template <bool FUSED>
+__global__ void __launch_bounds__(128) tc_split_merge_kernel(const DecodeParams p) {
+  const int64_t dix = blockIdx.x >> 5;
+  const int half = (blockIdx.x >> 4) & 1, chunk = blockIdx.x & 15;
+  const int h = threadIdx.x;
+  const int64_t* d = p.tc_desc + 2 + dix * 3;
+  const int64_t U1 = d[2];
+  if (U1 == 0) return;  // no split unit published here
+  const int64_t u = d[0], U0 = d[1];
+  const int64_t T = p.tc_desc[0], Pe = p.tc_desc[1];
+  const int64_t pf = min(Pe - 1, ((U0 + 1) * Pe - 1) / T);
+  const int64_t pl = min(Pe - 1, (U1 * Pe - 1) / T);
+  if ((dix >> 1) != pf) return;
+  const int H = p.heads;
+  float mx = -INFINITY;
+  for (int64_t q = pf; q <= pl; ++q) {
+    const int sq = (q * T / Pe) >= U0 ? 0 : 1;
+    mx = fmaxf(mx, __ldcg(p.tc_l + ((q * 2 + sq) * 2 + half) * 128 + h));
+  }
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float W = 0.f;
+  if (mx != -INFINITY) {
+    for (int64_t q = pf; q <= pl; ++q) {
+      const int sq = (q * T / Pe) >= U0 ? 0 : 1;
+      const float lq = __ldcg(p.tc_l + ((q * 2 + sq) * 2 + half) * 128 + h);
+      const float wq = fast_exp2((lq - mx) * kLog2e);
+      W += wq;
+      const float4* src = reinterpret_cast<const float4*>(
+          p.tc_o + ((q * 2 + sq) * 128 + h) * kDv + half * 256 + 16 * chunk);
+      float4 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __ldcg(src + i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[4 * i] = fmaf(wq, v[i].x, acc[4 * i]);
+        acc[4 * i + 1] = fmaf(wq, v[i].y, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(wq, v[i].z, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(wq, v[i].w, acc[4 * i + 3]);
+      }
+    }
+  }
+  if (h >= H) return;
+  const float iw = W > 0.f ? 1.0f / W : 0.f;
+  const int64_t oi = (u * H + h) * kDv + half * 256 + 16 * chunk;
+  if (FUSED) {
+    uint32_t b2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b2[i] = pack_bf16x2(acc[2 * i] * iw, acc[2 * i + 1] * iw);
+    uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi);
+    o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
+    o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
+  } else {
+    float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = make_float4(acc[4 * i] * iw, acc[4 * i + 1] * iw, acc[4 * i + 2] * iw, acc[4 * i + 3] * iw);
+  }
+  if (half == 0 && chunk == 0)
+    p.lse[u * H + h] = mx == -INFINITY ? -INFINITY : mx + __log2f(W) * kLn2;
+}
 
 int tc_pairs_for(int64_t units, int64_t tiles_bound) {
   static int sms = 0;
@@ -1187,7 +1193,10 @@ static cudaError_t tc_launch_one(const DecodeParams& p, cudaStream_t st) {
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p, lat, tail);
+  e = cudaLaunchKernelEx(&cfg, kern, p, lat, tail);
+  if (e != cudaSuccess || p.pairs < 2) return e;
+  tc_split_merge_kernel<FUSED><<<p.pairs * 2 * 32, 128, 0, st>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,

@@ -40,7 +40,7 @@ struct DecodeParams {
   int pairs;              // CTA pairs of the persistent grid
   float* tc_o;            // split-unit partials [pairs][2][128][512]
   float* tc_l;            // their LSEs [pairs][2][2][128]
-  unsigned* tc_cnt;       // tickets [units][2]
+  int64_t* tc_desc;       // [T, pairs owning tiles] + per (pair, slot) (unit, first tile, end tile)
   int32_t* err_timeout;   // error word for bounded-wait timeouts (whenever given)
 };
 
@@ -65,7 +65,7 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int kv_dtype, bool fused, 
 
 // Tensor-core decode (48..128 heads, page size 64).
 size_t tc_workspace_bytes(int64_t units, int pairs);
-size_t tc_ticket_bytes(int64_t units);
+size_t tc_clear_bytes(int pairs);
 void tc_bind_workspace(DecodeParams& p, void* ws);
 int tc_pairs_for(int64_t units, int64_t tiles_bound);
 int tc_tile_slots(int kv_dtype);

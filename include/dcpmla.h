@@ -233,8 +233,10 @@ int dcp_lse_merge(const float* part_out, const float* part_lse, int32_t dcp, int
  *   per-layer merge kernels (pack, exchange, LSE combine) is the biggest remaining
  *   latency item; this is its single-GPU form (all shards of a row in one launch).
  * args: fused meanings (global idx or global kv_len, [dcp] block tables, bf16 out).
- * Split-KV partials of a row are merged by the last CTA to finish (an atomic ticket in
- * the workspace; no waiting).  Errors as mla_decode_partial_lse.
+ * Rows whose work is divided between CTAs are merged without waiting: on the CUDA-core
+ * path by the last CTA to finish (an atomic ticket in the workspace), on the tensor-core
+ * path by a small merge kernel queued on the same stream after the decode.  Errors as
+ * mla_decode_partial_lse.
  */
 int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t interleave,
                          dcp_stream_t stream);
