@@ -211,6 +211,70 @@ def time_kv_cache_write(dcp, dev, peaks, stream, flush, steps):
             "frac": gbs / peaks["hbm_gbs"], "bound": "hbm", "launches_per_call": 1}
 
 
+def time_graph_step(dcp, dev, layers=4, reps=20):
+    """Launch overhead of a whole decode step on the small sparse workload (16 rows, 64 heads,
+    top-k 512, BF16, D = 4): `layers` fused calls, and the unfused form (one remap reused by
+    every layer, then per layer partials + merge), eager vs replayed as one CUDA graph."""
+    import synth
+    g = synth.cfg2_sparse_topk512(device=dev)
+    R, H, D, K = g.rows, g.heads, g.dcp, g.k
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+    loc = torch.empty((D, R, K), dtype=torch.int32, device=dev)
+    cnt = torch.empty((D, R), dtype=torch.int32, device=dev)
+    po = torch.empty((D, R, H, 512), dtype=torch.float32, device=dev)
+    pl = torch.empty((D, R, H), dtype=torch.float32, device=dev)
+
+    def ws_for(idx, count, o, l, n, fused):
+        a = dcp._decode_args(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq, g.sm_scale, idx,
+                             count, None, None, o, l, 0, False, None)
+        return torch.zeros(dcp.mla_decode_workspace_size(a, n, fused) + 256, dtype=torch.uint8, device=dev)
+
+    ws_f = ws_for(g.topk, None, out, lse, D, True)
+    ws_p = ws_for(loc, cnt, po, pl, D, False)
+
+    def fused():
+        for _ in range(layers):
+            dcp.mla_decode_dcp_fused(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq, g.sm_scale,
+                                     D, g.interleave, idx=g.topk, out=out, lse=lse, workspace=ws_f)
+
+    def unfused():
+        dcp.dcp_remap_topk(g.topk, D, g.interleave, local_idx=loc, count=cnt)
+        for _ in range(layers):
+            dcp.mla_decode_partial_lse(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq, g.sm_scale,
+                                       idx=loc, count=cnt, num_shards=D, out=po, lse=pl, workspace=ws_p)
+            dcp.dcp_lse_merge(po, pl, out=out, lse=lse)
+
+    res = {"workload": "sparse top-k 512, 64 heads, BF16 KV, 16 rows, DCP=4, %d layers per step" % layers}
+    for name, fn in (("fused", fused), ("unfused", unfused)):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        b.synchronize()
+        eager = a.elapsed_time(b) / reps
+        graph = torch.cuda.CUDAGraph()
+        st = torch.cuda.Stream(dev)
+        st.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(st):
+            with torch.cuda.graph(graph, stream=st):
+                fn()
+        torch.cuda.current_stream(dev).wait_stream(st)
+        graph.replay()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            graph.replay()
+        b.record()
+        b.synchronize()
+        res[name] = {"eager_us_per_layer": 1e3 * eager / layers,
+                     "graph_us_per_layer": 1e3 * a.elapsed_time(b) / reps / layers}
+    return res
+
+
 def cpu_baseline_sample(prob):
     """Oracle timed on host cores on a bounded sample of the same workload (rank 0, N = 1)."""
     import oracle
@@ -317,6 +381,7 @@ def main():
     torch.cuda.synchronize()
     unfused_ms = statistics.mean(a.elapsed_time(b) for a, b in uev)
     kvw = time_kv_cache_write(dcp, dev, peaks, stream, flush, args.steps)
+    graph_step = time_graph_step(dcp, dev)
 
     # end to end through the public API with host buffers: H2D of the step's inputs (queries,
     # top-k ids, row map, block tables) from pinned memory, D2H of the outputs
@@ -397,10 +462,12 @@ def main():
                     "launches_per_step": 3},
         "roofline": roof,
         "kv_cache_write": kvw,
+        "graph_step": graph_step,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
-        "gpu_launches": args.steps,
+        # per fused call: the persistent decode and the merge of rows cut between CTA pairs
+        "gpu_launches": 2 * args.steps,
     }
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(prob)
