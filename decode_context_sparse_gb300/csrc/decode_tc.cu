@@ -265,8 +265,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     sh.abort_flag = 0;
     fence_mbar_init();
     // the exchange inboxes expect one tile of partial logits each
-    mbar_arrive_expect_tx(&sh.in_full[0], 128 * TN * 4);
-    mbar_arrive_expect_tx(&sh.in_full[1], 128 * TN * 4);
+    mbar_arrive_expect_tx(&sh.in_full[0], L::X_BYTES);
+    mbar_arrive_expect_tx(&sh.in_full[1], L::X_BYTES);
   }
 
   // this pair's contiguous range of the tile sequence
@@ -738,25 +738,32 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         wn.next(p);
         load_q(wn.info.r);
       }
-      // this CTA's partial: to stage B through the local box (free once B(j-1) read it) ...
+      // this CTA's partial into the local box: read by stage B (free once B(j-1) read it)
+      // and copied to the peer's inbox (the warp's 32 rows in one bulk copy, free once the
+      // copy of tile j-1 has read them)
       const int x = buf;
       if (!mbar_wait(&sh.self_free, (j & 1) ^ 1, abort_flag)) break;
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
       float* srow = xself + h * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c)
         *reinterpret_cast<float4*>(srow + 4 * c) =
             make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.self_full);
-      // ... and to the peer's inbox
       if (!mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true)) break;
-      float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
-#pragma unroll
-      for (int c = 0; c < TN / 4; ++c)
-        st_async_v4(xrow + 4 * c, peer, __float_as_uint(s[4 * c]), __float_as_uint(s[4 * c + 1]),
-                    __float_as_uint(s[4 * c + 2]), __float_as_uint(s[4 * c + 3]), &sh.in_full[x]);
+      if (lane == 0) {
+        const int r0 = (warp & 3) * 32;
+        bulk_s2peer(xin + (x * 128 + r0) * L::XSTRIDE, xself + r0 * L::XSTRIDE,
+                    32 * L::XSTRIDE * 4, peer, &sh.in_full[x]);
+        bulk_commit();
+      }
       wa.next(p);
     }
+    if (lane == 0) bulk_wait0();  // no copy to the peer in flight when the CTA winds down
+    __syncwarp();
   } else if (warp >= 8) {
     // ============================================================ softmax stage B / epilogue
     const int h = tid - 256;  // head = TMEM lane
@@ -876,7 +883,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       }
       // inbox x is re-armed for the peer's next tile now (its phase is complete); each warp
       // hands its rows back to the peer at the end of this stage
-      if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&sh.in_full[x], 128 * TN * 4);
+      if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&sh.in_full[x], L::X_BYTES);
       // online softmax (base 2) with a lazily raised reference
       if (mask != 0xffffffffu) {
 #pragma unroll

@@ -343,6 +343,25 @@ __device__ __forceinline__ void st_async_v4(void* local, uint32_t rank, uint32_t
       : "memory");
 }
 
+// Shared memory of this CTA -> the mirrored address in CTA `rank` of the cluster (bytes a
+// multiple of 16, both ends 16-B aligned), completion counted in bytes on the barrier
+// mirroring `bar` in that CTA.  The source may be reused after bulk_wait_read0().
+__device__ __forceinline__ void bulk_s2peer(void* dst_mirror, const void* src, uint32_t bytes,
+                                            uint32_t rank, uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .b32 rd, rb;\n mapa.shared::cluster.u32 rd, %0, %3;\n"
+      " mapa.shared::cluster.u32 rb, %4, %3;\n"
+      " cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [rd], [%1], %2, [rb];\n}" ::
+          "r"(smem_u32(dst_mirror)),
+      "r"(smem_u32(src)), "r"(bytes), "r"(rank), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------------------------------ conversions
 // Two E4M3 codes -> two bf16 holding value * 2^-112, exactly: the hardware E4M3 -> F16
 // conversion is exact and every non-zero E4M3 value is a normal f16 with at most three
