@@ -116,7 +116,7 @@ def dist_env():
     return ws, rank, local
 
 
-TRAFFIC_BYTES_PER_ROW = (181.371392e6 + 18.441472e6) / 96
+TRAFFIC_BYTES_PER_ROW = (167.995392e6 + 15.666176e6) / 96
 
 
 def make_workload(dev, seqs=64):
@@ -438,7 +438,7 @@ def main():
         roof = {"bound": "hbm", "achieved": hbm_tbs * 1e3, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_tbs * 1e3 / peaks["hbm_gbs"]}
     # DRAM bytes (read + write) per launch from ncu (profiles/decode_tc_fused_topk2048_fp8_96rows.md:
-    # 181.4 MB + 18.4 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
+    # 168.0 MB + 15.7 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
     roof["traffic"] = TRAFFIC_BYTES_PER_ROW * R if prob.heads == 128 else None
     roof["traffic_unit"] = "bytes"
     roof["peak_src"] = peaks["src"]

@@ -41,7 +41,8 @@
 // (about 16 significant bits), so that s_lo * acc_lo + s_hi * acc_hi is the logit with
 // fp32 accuracy.  (|s_lo| below 2^-60 is taken as 2^-60 for this purpose; the latent
 // term it then adds is below 2^-51 |q|.)  For P V the block scales are folded into P:
-// O[:, lo] += (P s_lo) V_lo, O[:, hi] += (P s_hi) V_hi.
+// O[:, lo] += (P s_lo) V_lo, O[:, hi] += (P s_hi) V_hi, with P, s_lo and s_hi rounded to bf16
+// and multiplied as bf16 pairs (one more bf16 rounding of P than a BF16 cache gets).
 //
 // Work: a persistent grid of pairs; the concatenated sequence of 32-slot tiles of all
 // units (rows, or (shard, row) pairs) is cut into equal contiguous ranges, one per pair.
@@ -98,8 +99,8 @@ struct TcLay {
   // unpadded layout for the remote st.async stores.
   static constexpr int XSTRIDE = TN + 4;
   static constexpr int X_BYTES = 128 * XSTRIDE * 4;
-  // per K tile: logit scale lo | logit scale hi | P scale lo | P scale hi (the slot mask is
-  // kept in TcShared::kt_mask)
+  // per K tile: logit scale lo | logit scale hi (fp32, x sl2) | P scales s_lo, s_hi as bf16
+  // (the slot mask is kept in TcShared::kt_mask)
   static constexpr int META_BYTES = 4 * TN * 4;
   static constexpr int SBUF = C::NACC * TN;
   static constexpr int OFF_KT = 0;
@@ -622,8 +623,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
             float* mf = reinterpret_cast<float*>(meta);
             mf[rt] = sf * sl2;
             mf[TN + rt] = shi * sl2;
-            mf[2 * TN + rt] = slo;
-            mf[3 * TN + rt] = shi;
+            __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(mf + 2 * TN);
+            pb[rt] = __float2bfloat16_rn(slo);
+            pb[TN + rt] = __float2bfloat16_rn(shi);
           }
         }
       } else {
@@ -806,31 +808,37 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       const int64_t u = w.u;
       const int64_t oi = (u * H + h) * kDv + crank * 256;
       float* wso = p.tc_o + (((int64_t)pair * 2 + slot_idx) * 128 + h) * kDv + crank * 256;
-      for (int c = 0; c < 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(trow + kColO + 16 * c, v);
+      // four 16-column chunks per TMEM wait
+      for (int c4 = 0; c4 < 16; c4 += 4) {
+        uint32_t v[4][16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld16(trow + kColO + 16 * (c4 + k), v[k]);
         tmem_ld_wait();
-        float f[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]) * fix;
-        if (!complete) {
+        for (int k = 0; k < 4; ++k) {
+          const int c = c4 + k;
+          float f[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            __stcg(reinterpret_cast<float4*>(wso + 16 * c) + i,
-                   make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]));
-        } else if (h < H) {
-          if (FUSED) {
-            uint32_t b2[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) b2[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
-            o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
-            o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
-          } else {
-            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi + 16 * c);
+          for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[k][i]) * fix;
+          if (!complete) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              o[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+              __stcg(reinterpret_cast<float4*>(wso + 16 * c) + i,
+                     make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]));
+          } else if (h < H) {
+            if (FUSED) {
+              uint32_t b2[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) b2[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+              uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
+              o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
+              o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
+            } else {
+              float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi + 16 * c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                o[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            }
           }
         }
       }
@@ -955,16 +963,24 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
               make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
       } else {
-        const float4* pl4 = reinterpret_cast<const float4*>(meta + 8 * TN);
-        const float4* ph4 = pl4 + TN / 4;
+        const uint4* pl4 = reinterpret_cast<const uint4*>(meta + 8 * TN);   // bf16 s_lo x 32
+        const uint4* ph4 = pl4 + TN / 8;                                     // bf16 s_hi x 32
         uint32_t plo[TN / 2], phi[TN / 2];
 #pragma unroll
-        for (int i = 0; i < TN / 4; ++i) {
-          const float4 a = pl4[i], b = ph4[i];
-          plo[2 * i] = pack_bf16x2(pr[4 * i] * a.x, pr[4 * i + 1] * a.y);
-          plo[2 * i + 1] = pack_bf16x2(pr[4 * i + 2] * a.z, pr[4 * i + 3] * a.w);
-          phi[2 * i] = pack_bf16x2(pr[4 * i] * b.x, pr[4 * i + 1] * b.y);
-          phi[2 * i + 1] = pack_bf16x2(pr[4 * i + 2] * b.z, pr[4 * i + 3] * b.w);
+        for (int i = 0; i < TN / 8; ++i) {
+          const uint4 a = pl4[i], b = ph4[i];
+          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int m = 4 * i + k;
+            const uint32_t pp = pack_bf16x2(pr[2 * m], pr[2 * m + 1]);
+            __nv_bfloat162 r1 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pp),
+                                        *reinterpret_cast<const __nv_bfloat162*>(&aw[k]));
+            __nv_bfloat162 r2 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pp),
+                                        *reinterpret_cast<const __nv_bfloat162*>(&bw[k]));
+            plo[m] = *reinterpret_cast<uint32_t*>(&r1);
+            phi[m] = *reinterpret_cast<uint32_t*>(&r2);
+          }
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
