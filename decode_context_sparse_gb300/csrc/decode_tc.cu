@@ -70,12 +70,12 @@ struct TcCfg;
 // gather lands on a 128-B aligned stride.
 template <>
 struct TcCfg<DCP_KV_FP8_E4M3_S128> {
-  static constexpr int NACC = 2, NS = 3, NK = 4, NP = 2;
+  static constexpr int NACC = 2, NS = 2, NK = 4, NP = 1, NSB = 2;
   static constexpr int LAT_TOK = 256, TAIL_TOK = 144, TAIL_GSTRIDE = 640;
 };
 template <>
 struct TcCfg<DCP_KV_BF16> {
-  static constexpr int NACC = 1, NS = 2, NK = 4, NP = 2;
+  static constexpr int NACC = 1, NS = 2, NK = 4, NP = 1, NSB = 2;
   static constexpr int LAT_TOK = 512, TAIL_TOK = 64, TAIL_GSTRIDE = 256;
 };
 
@@ -110,7 +110,7 @@ struct TcLay {
   static constexpr int OFF_P = OFF_QR + QR_BYTES;
   static constexpr int OFF_X = OFF_P + C::NP * P_BYTES;
   static constexpr int OFF_SELF = OFF_X + 2 * X_BYTES;
-  static constexpr int SELF_BYTES = X_BYTES;  // the local box: same padded rows
+  static constexpr int SELF_BYTES = C::NSB * X_BYTES;  // local boxes: same padded rows
   static constexpr int OFF_META = OFF_SELF + SELF_BYTES;
   static constexpr int OFF_END = OFF_META + C::NK * META_BYTES;
   // at least 120 KB so that one CTA (and one TMEM owner) sits on an SM
@@ -123,7 +123,7 @@ struct TcLay {
 struct TcShared {
   uint64_t stg_full[4], stg_empty[4], kt_full[8], kt_empty[8];
   uint64_t s_full[2], p_full[2], pv_done[2], q_ready, in_full[2], out_free[2], drain;
-  uint64_t self_full, self_free;        // stage A -> stage B hand-over of this CTA's partial
+  uint64_t self_full[2], self_free[2];  // stage A -> stage B hand-over of this CTA's partial
   uint64_t s_free[2];                   // stage A has read a logit buffer out of TMEM
   uint32_t stg_mask[4];
   uint32_t kt_mask[8];        // valid-slot mask of each K tile
@@ -261,8 +261,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     mbar_init(&sh.pv_done[1], 1);
     mbar_init(&sh.q_ready, 4);
     mbar_init(&sh.drain, 1);
-    mbar_init(&sh.self_full, 4);
-    mbar_init(&sh.self_free, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.self_full[i], 4);
+      mbar_init(&sh.self_free[i], 4);
+    }
     sh.abort_flag = 0;
     fence_mbar_init();
     // the exchange inboxes expect one tile of partial logits each
@@ -744,21 +746,22 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       // and copied to the peer's inbox (the warp's 32 rows in one bulk copy, free once the
       // copy of tile j-1 has read them)
       const int x = buf;
-      if (!mbar_wait(&sh.self_free, (j & 1) ^ 1, abort_flag)) break;
-      if (lane == 0) bulk_wait_read0();
+      const int xs = j % C::NSB;  // local box of this tile
+      if (!mbar_wait(&sh.self_free[xs], ((j / C::NSB) & 1) ^ 1, abort_flag)) break;
+      if (lane == 0) bulk_wait_read<C::NSB - 1>();  // the copy of tile j - NSB has read it
       __syncwarp();
-      float* srow = xself + h * L::XSTRIDE;
+      float* srow = xself + (xs * 128 + h) * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c)
         *reinterpret_cast<float4*>(srow + 4 * c) =
             make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.self_full);
+      if (lane == 0) mbar_arrive(&sh.self_full[xs]);
       if (!mbar_wait(&sh.out_free[x], ((j >> 1) & 1) ^ 1, abort_flag, true)) break;
       if (lane == 0) {
         const int r0 = (warp & 3) * 32;
-        bulk_s2peer(xin + (x * 128 + r0) * L::XSTRIDE, xself + r0 * L::XSTRIDE,
+        bulk_s2peer(xin + (x * 128 + r0) * L::XSTRIDE, xself + (xs * 128 + r0) * L::XSTRIDE,
                     32 * L::XSTRIDE * 4, peer, &sh.in_full[x]);
         bulk_commit();
       }
@@ -866,9 +869,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       unsigned char* prow = smem + L::OFF_P + (j % C::NP) * L::P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
       float s[TN];
       // A(j) hands over after it saw the K tile complete: the tile's metadata is valid
-      if (!(ok = mbar_wait(&sh.self_full, j & 1, abort_flag))) break;
+      const int xs = j % C::NSB;
+      if (!(ok = mbar_wait(&sh.self_full[xs], (j / C::NSB) & 1, abort_flag))) break;
       const uint32_t mask = sh.kt_mask[j % NK];
-      const float* srow = xself + h * L::XSTRIDE;
+      const float* srow = xself + (xs * 128 + h) * L::XSTRIDE;
 #pragma unroll
       for (int c = 0; c < TN / 4; ++c) {
         const float4 v = *reinterpret_cast<const float4*>(srow + 4 * c);
@@ -878,7 +882,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         s[4 * c + 3] = v.w;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.self_free);
+      if (lane == 0) mbar_arrive(&sh.self_free[xs]);
       if (!(ok = mbar_wait(&sh.in_full[x], (j >> 1) & 1, abort_flag, true))) break;
       const float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
 #pragma unroll

@@ -361,6 +361,11 @@ __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// At most N of this thread's bulk-copy groups may still be reading their sources.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 // ------------------------------------------------------------------ conversions
 // Two E4M3 codes -> two bf16 holding value * 2^-112, exactly: the hardware E4M3 -> F16
