@@ -116,7 +116,7 @@ def dist_env():
     return ws, rank, local
 
 
-TRAFFIC_BYTES_PER_ROW = (167.995392e6 + 15.666176e6) / 96
+TRAFFIC_BYTES_PER_ROW = (167.1744e6 + 15.179776e6) / 96
 
 
 def make_workload(dev, seqs=64):

@@ -10,11 +10,12 @@
 // each row: CTA c owns latent dims [256c, 256c+256) and RoPE dims [512+32c, 512+32c+32)
 // of every key, computes the partial logits q.k over its 288 dims and the output columns
 // of its 256 value dims.  The two partial logit tiles are exchanged through distributed
-// shared memory (st.async counted on the peer's mbarrier) and both CTAs run the same
-// softmax.
+// shared memory (one bulk copy per warp, completing on the peer's mbarrier) and both CTAs
+// run the same softmax.
 //
 // Per CTA (512 threads), tiles of 32 key slots:
-//   warps 1-3   loaders (tiles round-robin; as many as staging slots, at most three):
+//   warps 1-3   loaders (tiles round-robin; as many as staging slots, at most three; the
+//               others idle):
 //               slot id -> owner shard / local slot -> page
 //               (a three-stage software pipeline over the dependent loads), then 4-row TMA
 //               gathers of this CTA's latent half and of the row tail into a staging ring;
@@ -24,15 +25,14 @@
 //   warps 4-7   converters: staging -> SWIZZLE_128B bf16 K tile (FP8: E4M3 -> bf16,
 //               exact), zero rows for padding, per-slot scales;
 //   warps 12-15 softmax stage A: thread h owns head h (TMEM lane h): reads its logits of
-//               a tile, scales them, hands this CTA's partial to stage B through shared
-//               memory and to the peer CTA through distributed shared memory; loads Q;
+//               a tile, scales them, hands this CTA's partial to stage B through a local
+//               box in shared memory and copies the box to the peer CTA's inbox; loads Q;
 //   warps 8-11  softmax stage B: adds the two partials, online softmax in base 2 with a
 //               lazily raised reference max (the output is rescaled only when the max
-//               grows by more than 2^8), writes P as bf16 into TMEM, and at the end of a
-//               row normalises O and writes it out (or merges split rows).
-// TMEM columns: O [0,256) | Q latent [256,384) | two logit buffers from 384.  P tiles are
-// double-buffered in shared memory, so a logit buffer is free again as soon as stage A has
-// read it.
+//               grows by more than 2^8), writes P as bf16 into shared memory, and at the
+//               end of a row normalises O and writes it out (or a partial of a split row).
+// TMEM columns: O [0,256) | Q latent [256,384) | two logit buffers from 384.  P lives in
+// shared memory, so a logit buffer is free again as soon as stage A has read it.
 //
 // FP8 numerics.  Each CTA's 256 latent dims are two 128-blocks with their own scales
 // s_lo, s_hi, so the logit needs two accumulators: acc_lo = q_lo . k_lo and
@@ -46,9 +46,10 @@
 //
 // Work: a persistent grid of pairs; the concatenated sequence of 32-slot tiles of all
 // units (rows, or (shard, row) pairs) is cut into equal contiguous ranges, one per pair.
-// A unit cut by a range edge leaves fp32 partials in the workspace; the last pair to
-// finish it (atomic ticket, no waiting) merges them.  Every wait is bounded; a wait that
-// expires sets an abort flag, the CTA winds down and DCP_ERRBIT_TIMEOUT is reported.
+// A unit cut by a range edge leaves fp32 partials and a descriptor in the workspace;
+// tc_split_merge_kernel, launched after this kernel on the same stream, merges them.  Every
+// wait is bounded; a wait that expires sets an abort flag, the CTA winds down and
+// DCP_ERRBIT_TIMEOUT is reported.
 #include <cuda.h>
 #include <stdlib.h>
 
