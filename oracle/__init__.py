@@ -13,11 +13,15 @@ Functions (each follows a passage of the public pages on DCP, cited in the C sou
   * :func:`remap`         -- top-k slot remap per shard (stable compaction + count);
   * :func:`attention`     -- sparse or dense MLA decode attention with LSE, unsharded or
     restricted to one shard, brute force over the selected slots;
-  * :func:`merge`         -- LSE merge of shard partials with the all-empty case.
+  * :func:`merge`         -- LSE merge of shard partials with the all-empty case;
+  * :func:`e4m3_encode`, :func:`kv_write` -- FP8 quantisation and the DCP KV-cache write;
+  * ``oracle.topk``        -- the DSA top-k producer under DCP (per-shard candidates and
+    their merge; numpy, see that module).
 
-Parity status: every function above is pinned by ``tests/test_oracle_pins.py`` against
-closed forms, hand-worked fixtures (``tests/golden/``), brute-force enumeration and
-invariants; none is "parity unpinned".
+Parity status: every function above is pinned against closed forms, hand-worked fixtures
+(``tests/golden/``), brute-force enumeration and invariants by ``tests/test_oracle_pins.py``,
+``tests/test_oracle_kv_write_pins.py`` and ``tests/test_oracle_topk_pins.py``; none is
+"parity unpinned".
 """
 from __future__ import annotations
 
@@ -243,3 +247,6 @@ def kv_write(kv, seq, pos, pool, kv_dtype: int, block_table, dcp: int, interleav
                                    int(shard), _ptr(out), num_pages, int(kv_dtype), page_size,
                                    _ptr(bt), bt.shape[1], bt.shape[2], ctypes.byref(skipped))
     return out, int(written), int(skipped.value)
+
+
+from . import topk  # noqa: E402  (numpy-only; no C build needed)
