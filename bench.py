@@ -211,6 +211,71 @@ def time_kv_cache_write(dcp, dev, peaks, stream, flush, steps):
             "frac": gbs / peaks["hbm_gbs"], "bound": "hbm", "launches_per_call": 1}
 
 
+def time_topk_producer(dcp, dev, peaks, stream, flush, steps):
+    """The DSA top-k producer of the decode batch: every shard's candidate list (8 shards x
+    384 rows, 16384 local slots each, k = 2048) and their merge into the rows' global top-k,
+    timed like the decode (events, L2 flushed between calls).  Algorithmic bytes: the local
+    scores read (4 B per local slot) and the lists written (8 B per candidate); the lists
+    read again (8 B) and the top-k written (4 B per entry + 4 B count per row)."""
+    import synth
+    p = synth.topk_producer_topk2048(device=dev)
+    D, k = p.dcp, p.k
+    R = p.row_len.numel()
+    ll = dcp.dcp_local_lengths(p.row_len, D, p.interleave)
+    cs = torch.empty((D, R, k), dtype=torch.float32, device=dev)
+    ci = torch.empty((D, R, k), dtype=torch.int32, device=dev)
+    top = torch.empty((R, k), dtype=torch.int32, device=dev)
+    cnt = torch.empty((R,), dtype=torch.int32, device=dev)
+
+    def local():
+        dcp.dcp_topk_local(p.scores, ll, k, D, p.interleave, cand_score=cs, cand_idx=ci)
+
+    def merge():
+        dcp.dcp_topk_merge(cs, ci, k, topk=top, count=cnt)
+
+    for _ in range(3):
+        local()
+        merge()
+    n = max(3, steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    for a, b, c in ev:
+        flush.fill_(4)
+        a.record(stream)
+        local()
+        b.record(stream)
+        merge()
+        c.record(stream)
+    torch.cuda.synchronize()
+    ms_l = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    ms_m = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    b_local = int(ll.sum().item()) * 4 + D * R * 4 + D * R * k * 8
+    b_merge = D * R * k * 8 + R * k * 4 + R * 4
+    g_l = b_local / (ms_l / 1e3) / 1e9
+    g_m = b_merge / (ms_m / 1e3) / 1e9
+    g = (b_local + b_merge) / ((ms_l + ms_m) / 1e3) / 1e9
+    return {"workload": "DSA top-k producer, 8 shards x 384 rows x 16384 local slots, k 2048",
+            "us_local": 1e3 * ms_l, "us_merge": 1e3 * ms_m,
+            "algorithmic_bytes_local": b_local, "algorithmic_bytes_merge": b_merge,
+            "achieved_gbs_local": g_l, "achieved_gbs_merge": g_m, "achieved_gbs": g,
+            "peak_gbs": peaks["hbm_gbs"], "frac": g / peaks["hbm_gbs"], "bound": "hbm",
+            "launches_per_call": 2}
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (x itself without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, steps: int, max_total_ms: float, world: int) -> float:
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return world * units_per_rank * steps / (max_total_ms / 1e3)
+
+
 def time_graph_step(dcp, dev, layers=4, reps=20):
     """Launch overhead of a whole decode step on the small sparse workload (16 rows, 64 heads,
     top-k 512, BF16, D = 4): `layers` fused calls, and the unfused form (one remap reused by
@@ -345,15 +410,13 @@ def main():
         step()
         evs[i][1].record(stream)
     torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
     clocks = sampler.stop()
     times_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = sum(times_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(times_ms), dev)
     avg_ms = total_ms / args.steps
-    value = ws * R * args.steps / (total_ms / 1e3)
+    value = whole_job_rate(R, args.steps, total_ms, ws)
 
     # unfused pipeline (remap -> partials -> merge), same workload, same timing rules
     D = prob.dcp
@@ -381,6 +444,7 @@ def main():
     torch.cuda.synchronize()
     unfused_ms = statistics.mean(a.elapsed_time(b) for a, b in uev)
     kvw = time_kv_cache_write(dcp, dev, peaks, stream, flush, args.steps)
+    topk_prod = time_topk_producer(dcp, dev, peaks, stream, flush, args.steps)
     graph_step = time_graph_step(dcp, dev)
 
     # end to end through the public API with host buffers: H2D of the step's inputs (queries,
@@ -418,7 +482,7 @@ def main():
         e2e_ms.append(a.elapsed_time(b))
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_topk, h_rs, h_bt))
     d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
-    e2e_val = ws * R * len(e2e_ms) / (sum(e2e_ms) / 1e3)
+    e2e_val = whole_job_rate(R, len(e2e_ms), max_over_ranks(sum(e2e_ms), dev), ws)
 
     if rank != 0:
         if ws > 1:
@@ -438,7 +502,7 @@ def main():
         roof = {"bound": "hbm", "achieved": hbm_tbs * 1e3, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_tbs * 1e3 / peaks["hbm_gbs"]}
     # DRAM bytes (read + write) per launch from ncu (profiles/decode_tc_fused_topk2048_fp8_96rows.md:
-    # 168.0 MB + 15.7 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
+    # 167.2 MB + 15.2 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
     roof["traffic"] = TRAFFIC_BYTES_PER_ROW * R if prob.heads == 128 else None
     roof["traffic_unit"] = "bytes"
     roof["peak_src"] = peaks["src"]
@@ -462,6 +526,7 @@ def main():
                     "launches_per_step": 3},
         "roofline": roof,
         "kv_cache_write": kvw,
+        "topk_producer": topk_prod,
         "graph_step": graph_step,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": h2d,

@@ -35,7 +35,8 @@ TOKEN_BYTES = {DCP_KV_BF16: 1152, DCP_KV_FP8_E4M3_S128: 656}
 # every symbol include/dcpmla.h declares
 EXPORTS = ("dcp_status_string", "dcp_abi_version", "dcp_remap_topk", "dcp_local_lengths",
            "mla_decode_partial_lse", "dcp_lse_merge", "mla_decode_dcp_fused",
-           "mla_decode_workspace_size", "mla_decode_dcp_fused_noalloc", "dcp_kv_cache_write")
+           "mla_decode_workspace_size", "mla_decode_dcp_fused_noalloc", "dcp_kv_cache_write",
+           "dcp_topk_local", "dcp_topk_merge")
 DCP_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -95,6 +96,10 @@ def load(path: str = LIB_PATH):
     lib.dcp_kv_cache_write.restype = ctypes.c_int
     lib.dcp_kv_cache_write.argtypes = [V, I64, V, V, I32, I32, I32, V, I64, I32, I32, V, I32, I32,
                                        I32, V, V]
+    lib.dcp_topk_local.restype = ctypes.c_int
+    lib.dcp_topk_local.argtypes = [V, I64, I32, V, I32, I32, I32, I32, V, V, V]
+    lib.dcp_topk_merge.restype = ctypes.c_int
+    lib.dcp_topk_merge.argtypes = [V, V, I32, I64, I32, I32, V, V, V]
     lib.mla_decode_workspace_size.restype = SZ
     lib.mla_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32]
     if lib.dcp_abi_version() != DCP_ABI_VERSION:
@@ -165,6 +170,65 @@ def dcp_local_lengths(global_len: torch.Tensor, dcp: int, interleave: int, shard
     _check(load().dcp_local_lengths(_ptr(global_len), rows, dcp, interleave, shard,
                                     _ptr(local_len), _stream(stream)), "dcp_local_lengths")
     return local_len
+
+
+# ------------------------------------------------------------------------------ DSA top-k producer
+def dcp_topk_local(scores: torch.Tensor, local_len: torch.Tensor, k: int, dcp: int, interleave: int,
+                   shard: int = -1, cand_score: Optional[torch.Tensor] = None,
+                   cand_idx: Optional[torch.Tensor] = None, stream=None):
+    """Each shard's best k local slots as global ids ascending with their scores:
+    scores [n_in, R, stride] fp32, local_len [n_in, R] int32 ->
+    (cand_score [n_in, R, k] fp32, cand_idx [n_in, R, k] int32)."""
+    if scores.dtype != torch.float32 or scores.dim() != 3:
+        raise ValueError("scores must be [n_in, rows, stride] float32")
+    _i32(local_len, "local_len")
+    n_in, rows, stride = scores.shape
+    if n_in != (dcp if shard < 0 else 1) or local_len.shape != (n_in, rows):
+        raise ValueError("scores / local_len do not match dcp and shard")
+    if cand_score is None:
+        cand_score = torch.empty((n_in, rows, k), dtype=torch.float32, device=scores.device)
+    if cand_idx is None:
+        cand_idx = torch.empty((n_in, rows, k), dtype=torch.int32, device=scores.device)
+    _check(load().dcp_topk_local(_ptr(scores), rows, stride, _ptr(local_len), k, dcp, interleave,
+                                 shard, _ptr(cand_score), _ptr(cand_idx), _stream(stream)),
+           "dcp_topk_local")
+    return cand_score, cand_idx
+
+
+def dcp_topk_merge(cand_score: torch.Tensor, cand_idx: torch.Tensor, k: Optional[int] = None,
+                   topk: Optional[torch.Tensor] = None, count: Optional[torch.Tensor] = None,
+                   stream=None):
+    """Global top-k of a row from the D shards' lists [D, R, k_in] ->
+    (topk [R, k] int32 ascending then -1, count [R] int32)."""
+    if cand_score.dtype != torch.float32 or cand_score.dim() != 3:
+        raise ValueError("cand_score must be [dcp, rows, k_in] float32")
+    _i32(cand_idx, "cand_idx")
+    D, rows, k_in = cand_score.shape
+    if cand_idx.shape != cand_score.shape:
+        raise ValueError("cand_idx must match cand_score")
+    k = k_in if k is None else k
+    if topk is None:
+        topk = torch.empty((rows, k), dtype=torch.int32, device=cand_score.device)
+    if count is None:
+        count = torch.empty((rows,), dtype=torch.int32, device=cand_score.device)
+    _check(load().dcp_topk_merge(_ptr(cand_score), _ptr(cand_idx), D, rows, k_in, k, _ptr(topk),
+                                 _ptr(count), _stream(stream)), "dcp_topk_merge")
+    return topk, count
+
+
+def dcp_topk_gather(cand_score: torch.Tensor, cand_idx: torch.Tensor, group=None):
+    """The exchange step of the top-k producer on several ranks: rank s holds shard s's lists
+    [1, R, k] (or [R, k]); returns every shard's lists [D, R, k] in shard (= rank) order,
+    the input layout of dcp_topk_merge.  One all-gather per tensor of the process group."""
+    import torch.distributed as dist
+    D = dist.get_world_size(group)
+    cs = cand_score.reshape(cand_score.shape[-2:]).contiguous()
+    ci = cand_idx.reshape(cand_idx.shape[-2:]).contiguous()
+    out_s = torch.empty((D,) + tuple(cs.shape), dtype=cs.dtype, device=cs.device)
+    out_i = torch.empty((D,) + tuple(ci.shape), dtype=ci.dtype, device=ci.device)
+    dist.all_gather(list(out_s.unbind(0)), cs, group=group)
+    dist.all_gather(list(out_i.unbind(0)), ci, group=group)
+    return out_s, out_i
 
 
 # ------------------------------------------------------------------------------ cache write

@@ -167,6 +167,55 @@ int dcp_kv_cache_write(const void* kv, int64_t n, const int32_t* seq, const int3
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int dcp_topk_local(const float* scores, int64_t rows, int32_t score_stride,
+                   const int32_t* local_len, int32_t k, int32_t dcp, int32_t interleave,
+                   int32_t shard, float* cand_score, int32_t* cand_idx, dcp_stream_t stream) {
+  if (!scores || !local_len || !cand_score || !cand_idx) return DCP_ERR_INVALID_ARG;
+  if (rows < 0 || score_stride < 1 || k < 1 || k > DCP_MAX_TOPK) return DCP_ERR_INVALID_ARG;
+  if (!valid_rule(dcp, interleave) || shard < -1 || shard >= dcp) return DCP_ERR_INVALID_ARG;
+  if (!aligned(scores, 4) || !aligned(cand_score, 4) || !aligned(local_len, 4) ||
+      !aligned(cand_idx, 4))
+    return DCP_ERR_INVALID_ARG;
+  const int64_t n_in = shard < 0 ? dcp : 1;
+  if (rows * n_in > INT32_MAX) return DCP_ERR_INVALID_ARG;
+  // the global slot of the last local slot of a row must be an int32
+  const int64_t span = ((int64_t)(score_stride - 1) / interleave + 1) * interleave * dcp;
+  if (span - 1 > INT32_MAX) return DCP_ERR_INVALID_ARG;
+  TopkParams p{};
+  p.score = scores;
+  p.len = local_len;
+  p.rows = rows;
+  p.stride = score_stride;
+  p.D = dcp;
+  p.I = interleave;
+  p.shard = shard;
+  p.k = k;
+  p.cand_score = cand_score;
+  p.cand_idx = cand_idx;
+  return status_of(launch_topk_local(p, (int)n_in, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dcp_topk_merge(const float* cand_score, const int32_t* cand_idx, int32_t dcp, int64_t rows,
+                   int32_t k_in, int32_t k, int32_t* topk, int32_t* count, dcp_stream_t stream) {
+  if (!cand_score || !cand_idx || !topk) return DCP_ERR_INVALID_ARG;
+  if (dcp < 1 || dcp > DCP_MAX_SHARDS || rows < 0 || rows > INT32_MAX) return DCP_ERR_INVALID_ARG;
+  if (k_in < 1 || k < 1 || k > DCP_MAX_TOPK || (int64_t)dcp * k_in > INT32_MAX)
+    return DCP_ERR_INVALID_ARG;
+  if (!aligned(cand_score, 4) || !aligned(cand_idx, 4) || !aligned(topk, 4) ||
+      !aligned(count, 4))
+    return DCP_ERR_INVALID_ARG;
+  TopkParams p{};
+  p.score = cand_score;
+  p.ids = cand_idx;
+  p.rows = rows;
+  p.stride = k_in;
+  p.D = dcp;
+  p.k = k;
+  p.topk = topk;
+  p.count = count;
+  return status_of(launch_topk_merge(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int dcp_lse_merge(const float* part_out, const float* part_lse, int32_t dcp, int64_t rows,
                   int32_t heads, int32_t dv, void* out, float* lse, dcp_stream_t stream) {
   if (!part_out || !part_lse || !out || !lse) return DCP_ERR_INVALID_ARG;

@@ -52,6 +52,24 @@ cudaError_t launch_kv_write(const void* kv, int64_t n, const int32_t* seq, const
                             int D, int I, int shard, void* pool, int64_t num_pages, int kv_dtype,
                             const int32_t* bt, int num_seqs, int bt_stride, int32_t* err,
                             cudaStream_t st);
+// DSA top-k producer: per-shard candidate lists and their merge (csrc/topk.cu).
+constexpr int kTkStageMax = 16384;  // list entries staged in shared memory (longer: L2)
+struct TopkParams {
+  const float* score;     // candidates: [n_in][rows][stride]; merge: [D][rows][stride]
+  const int32_t* ids;     // merge: [D][rows][stride] global slot ids
+  const int32_t* len;     // candidates: [n_in][rows] local lengths
+  int64_t rows;
+  int stride;             // candidates: score row stride; merge: entries per shard list
+  int D, I, shard;        // candidates: owner rule and shard (-1: list block o is shard o)
+  int k;
+  int stage, kp;          // set by the launchers: staged entries, sort size (merge)
+  float* cand_score;      // candidates: [n_in][rows][k]
+  int32_t* cand_idx;
+  int32_t* topk;          // merge: [rows][k]
+  int32_t* count;         // merge: [rows] or NULL
+};
+cudaError_t launch_topk_local(TopkParams p, int n_in, cudaStream_t st);
+cudaError_t launch_topk_merge(TopkParams p, cudaStream_t st);
 cudaError_t launch_lse_merge(const float* part_out, const float* part_lse, int D, int64_t rows,
                              int heads, int dv, void* out, float* lse, cudaStream_t st);
 

@@ -138,6 +138,57 @@ int dcp_kv_cache_write(const void* kv, int64_t n, const int32_t* seq, const int3
                        int32_t checked, int32_t* err_flag, dcp_stream_t stream);
 
 /*
+ * dcp_topk_local -- DSA top-k producer under DCP, step 1: each shard's candidate list.
+ * Passages: LMDeploy PR #4952 "support decode context parallelism for PyTorch MLA",
+ *   Summary (for decode, DSA merges local candidates into the global top-k) and its file
+ *   list (the DCP top-k kernel packs the distributed candidates and merges them); SGLang
+ *   PR #36990, item 2 (with the index cache split across ranks, every indexer layer merges
+ *   the ranks' local top-k candidates).
+ *
+ * scores     (device) [n_in][rows][score_stride] fp32: the indexer score of local slot l of
+ *            each row on each shard, l < local_len (later entries are not read); n_in = D
+ *            for shard = -1 (block o is shard o), else 1.
+ * local_len  (device) [n_in][rows] int32: local slots of the row on that shard (clamped to
+ *            [0, score_stride]); dcp_local_lengths gives them from the visible lengths.
+ * k          candidates per list, 1..DCP_MAX_TOPK.
+ * dcp, interleave, shard  the owner rule; local slot l of shard s is the l-th slot, in
+ *            increasing global order, that the rule gives s, i.e. global slot
+ *            (l / I)*I*D + s*I + l % I.
+ * cand_score (device) [n_in][rows][k] fp32 and cand_idx (device) [n_in][rows][k] int32: the
+ *            selected slots as GLOBAL slot ids in increasing order with their scores (the
+ *            input values), then (-inf, -1).
+ * Selection: a slot is a candidate unless its score is NaN or -inf; candidates rank by
+ *   score, higher first (-0 equals +0), equal scores by the smaller global slot id, and the
+ *   first min(k, candidates) are selected.  Comparisons only: bit-identical to that rule.
+ * Errors: DCP_ERR_INVALID_ARG for null or misaligned (4-B) pointers, rows < 0,
+ *   score_stride < 1, k outside [1, DCP_MAX_TOPK], a bad owner rule or shard, or global
+ *   slot ids past INT32_MAX.  rows = 0 is a no-op.
+ */
+int dcp_topk_local(const float* scores, int64_t rows, int32_t score_stride,
+                   const int32_t* local_len, int32_t k, int32_t dcp, int32_t interleave,
+                   int32_t shard, float* cand_score, int32_t* cand_idx, dcp_stream_t stream);
+
+/*
+ * dcp_topk_merge -- DSA top-k producer under DCP, step 2: the global top-k of a row from
+ * the D shards' candidate lists (passages as dcp_topk_local).
+ *
+ * cand_score, cand_idx (device) [dcp][rows][k_in]: every shard's list as dcp_topk_local
+ *            writes it (on several GPUs, gathered from the D ranks); an id < 0 is padding.
+ * topk       (device) [rows][k] int32: the selected global slot ids in increasing order,
+ *            then -1 -- the input layout of dcp_remap_topk and of the fused decode.
+ * count      (device, may be NULL) [rows] int32: number of selected slots.
+ * Selection as dcp_topk_local over the D*k_in candidates of the row.  Since every global
+ *   top-k slot is among its own shard's best k, for k <= k_in the result is the top-k of
+ *   the unsharded scores.  Ids must be distinct within a row (else which of the tied
+ *   entries are kept is unspecified; at most k are written).
+ * Errors: DCP_ERR_INVALID_ARG for null or misaligned pointers, dcp outside
+ *   [1, DCP_MAX_SHARDS], rows < 0, k_in < 1, k outside [1, DCP_MAX_TOPK], dcp*k_in past
+ *   INT32_MAX.  rows = 0 is a no-op.
+ */
+int dcp_topk_merge(const float* cand_score, const int32_t* cand_idx, int32_t dcp, int64_t rows,
+                   int32_t k_in, int32_t k, int32_t* topk, int32_t* count, dcp_stream_t stream);
+
+/*
  * Arguments of the decode entry points.  Field meaning differs between the per-shard
  * call (mla_decode_partial_lse) and the fused call (mla_decode_dcp_fused) where noted.
  */

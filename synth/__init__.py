@@ -284,3 +284,48 @@ def cfg4_remap_merge(dcp, device="cpu", rows=256, k=2048, heads=128, seq_len=131
         part_lse = torch.where(empty.unsqueeze(-1), torch.full_like(part_lse, -math.inf), part_lse)
         part_out = torch.where(empty[..., None, None], torch.zeros_like(part_out), part_out)
     return RemapMergeProblem(dcp, interleave, topk.contiguous(), part_out, part_lse)
+
+
+# ---------------------------------------------------------------------------------------
+# DSA indexer scores for the top-k producer (per-shard candidate lists and their merge).
+# ---------------------------------------------------------------------------------------
+
+@dataclass
+class TopkProducerProblem:
+    """Indexer scores of every shard's local slots for a batch of decode rows."""
+    dcp: int
+    interleave: int
+    k: int
+    row_len: torch.Tensor     # [R] int32 visible global length of each row
+    scores: torch.Tensor      # [D, R, stride] fp32, N(0,1); entries past a row's local length unused
+    stride: int               # >= the longest local length (an upper bound, see local_len_bound)
+
+
+def local_len_bound(seq_len: int, dcp: int, interleave: int) -> int:
+    """Upper bound on the slots any one shard holds of seq_len global slots."""
+    return interleave * -(-seq_len // (interleave * dcp))
+
+
+def index_scores(shards: int, rows: int, stride: int, gen, ties: bool = False,
+                 masked: float = 0.0) -> torch.Tensor:
+    """Indexer scores N(0,1) fp32 [shards, rows, stride]; ties=True rounds them to
+    multiples of 1/4 (many equal scores); a fraction `masked` is set to -inf."""
+    s = torch.randn((shards, rows, stride), generator=gen, device=gen.device)
+    if ties:
+        s = torch.round(s * 4.0) / 4.0
+    if masked > 0:
+        s = torch.where(torch.rand(s.shape, generator=gen, device=gen.device) < masked,
+                        torch.full_like(s, float("-inf")), s)
+    return s.contiguous()
+
+
+def topk_producer_topk2048(device="cpu", seqs=64, mtp=6, seq_len=131072, dcp=8, k=2048,
+                           interleave=1, seed=6):
+    """The top-k 2048 decode batch's producer: 64 sequences x 6 MTP rows (row i of a
+    sequence sees seq_len - 5 + i slots), D = 8 shards, N(0,1) indexer scores."""
+    gen = _gen(seed, device)
+    row_len = torch.tensor([seq_len - (mtp - 1) + i for _ in range(seqs) for i in range(mtp)],
+                           dtype=torch.int32, device=device)
+    stride = local_len_bound(seq_len, dcp, interleave)
+    scores = index_scores(dcp, seqs * mtp, stride, gen)
+    return TopkProducerProblem(dcp, interleave, k, row_len, scores, stride)

@@ -132,3 +132,39 @@ def test_kv_cache_write_rejects_bad_arguments(lib):
     assert run(page_size=32) == dcp.DCP_ERR_UNSUPPORTED
     assert run(kv_dtype=3) == dcp.DCP_ERR_UNSUPPORTED
     assert run(n=0) == dcp.DCP_OK    # nothing to do, nothing launched
+
+
+def test_topk_entries_reject_bad_arguments(lib):
+    import decode_context_sparse_gb300 as dcp
+    g = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 2)
+    loc = lib.dcp_topk_local
+    ok = dict(sc=g, rows=4, stride=1000, ln=g, k=16, dcp=2, il=1, shard=-1, cs=g, ci=g)
+
+    def run_l(**kw):
+        a = dict(ok, **kw)
+        return loc(a["sc"], a["rows"], a["stride"], a["ln"], a["k"], a["dcp"], a["il"], a["shard"],
+                   a["cs"], a["ci"], None)
+    E = dcp.DCP_ERR_INVALID_ARG
+    assert run_l(sc=None) == E
+    assert run_l(ci=None) == E
+    assert run_l(sc=bad) == E                       # misaligned scores
+    assert run_l(rows=-1) == E
+    assert run_l(stride=0) == E
+    assert run_l(k=0) == E and run_l(k=dcp.DCP_MAX_TOPK + 1) == E
+    assert run_l(dcp=0) == E and run_l(shard=2) == E and run_l(il=0) == E
+    assert run_l(stride=1 << 30, dcp=8) == E        # global slot ids past INT32_MAX
+    assert run_l(rows=0) == dcp.DCP_OK              # nothing to do, nothing launched
+    mrg = lib.dcp_topk_merge
+    okm = dict(cs=g, ci=g, dcp=8, rows=4, kin=2048, k=2048, top=g, cnt=g)
+
+    def run_m(**kw):
+        a = dict(okm, **kw)
+        return mrg(a["cs"], a["ci"], a["dcp"], a["rows"], a["kin"], a["k"], a["top"], a["cnt"], None)
+    assert run_m(cs=None) == E and run_m(top=None) == E
+    assert run_m(dcp=0) == E and run_m(dcp=dcp.DCP_MAX_SHARDS + 1) == E
+    assert run_m(rows=-1) == E and run_m(kin=0) == E and run_m(k=0) == E
+    assert run_m(k=dcp.DCP_MAX_TOPK + 1) == E
+    assert run_m(dcp=64, kin=1 << 26) == E          # D * k_in past INT32_MAX
+    assert run_m(top=bad) == E
+    assert run_m(rows=0) == dcp.DCP_OK
