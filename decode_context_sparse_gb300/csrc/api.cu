@@ -192,6 +192,7 @@ int dcp_topk_local(const float* scores, int64_t rows, int32_t score_stride,
   p.k = k;
   p.cand_score = cand_score;
   p.cand_idx = cand_idx;
+  p.vec = aligned(scores, 16) && score_stride % 4 == 0;
   return status_of(launch_topk_local(p, (int)n_in, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -213,6 +214,7 @@ int dcp_topk_merge(const float* cand_score, const int32_t* cand_idx, int32_t dcp
   p.k = k;
   p.topk = topk;
   p.count = count;
+  p.vec = aligned(cand_score, 16) && aligned(cand_idx, 16) && k_in % 4 == 0;
   return status_of(launch_topk_merge(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -62,6 +62,7 @@ struct TopkParams {
   int stride;             // candidates: score row stride; merge: entries per shard list
   int D, I, shard;        // candidates: owner rule and shard (-1: list block o is shard o)
   int k;
+  int vec;                // lists 16-B aligned with a multiple of 4 entries per row / list
   int stage, kp;          // set by the launchers: staged entries, sort size (merge)
   float* cand_score;      // candidates: [n_in][rows][k]
   int32_t* cand_idx;

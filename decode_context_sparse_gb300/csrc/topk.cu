@@ -25,16 +25,27 @@
 
 namespace dcp {
 
+constexpr int kTkMaxDevices = 64;
 constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkBins = 2048;
+constexpr int kTkRound = 4 * kTkThreads;  // entries per round: four consecutive per thread
+constexpr int kTkLoadRounds = 4;          // rounds whose loads are issued together
+constexpr int kTkBlockRounds = kTkStageMax / kTkRound;  // rounds per compaction block
+static_assert(kTkStageMax % kTkRound == 0, "staging holds whole rounds");
 
 // Order-preserving image of an fp32 score; 0 for the entries that are never selected.
 __device__ __forceinline__ uint32_t score_key(float s) {
-  const uint32_t u = __float_as_uint(s);
-  if (s != s || u == 0xff800000u) return 0u;   // NaN, -inf
-  if (u == 0x80000000u) return 0x80000000u;     // -0 ranks as +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  uint32_t u = __float_as_uint(s);
+  const bool valid = s == s && u != 0xff800000u;  // not NaN, not -inf
+  u = u == 0x80000000u ? 0u : u;                   // -0 ranks as +0
+  const uint32_t flip = (u & 0x80000000u) ? 0xffffffffu : 0x80000000u;
+  return valid ? (u ^ flip) : 0u;
+}
+
+// The fp32 score of a key (inverse of score_key for keys other than 0).
+__device__ __forceinline__ float key_score(uint32_t h) {
+  return __uint_as_float((h & 0x80000000u) ? (h ^ 0x80000000u) : ~h);
 }
 
 // Entry i of one list.
@@ -44,7 +55,9 @@ struct TkList {
   const int32_t* id;   // merge: shard 0's ids of the row
   int64_t dstride;     // merge: elements between two shards' lists
   int kin;             // merge: entries per shard list
+  int n;               // entries
   int D, I, s;         // candidates: owner rule and shard
+  bool vec;            // four consecutive entries from one 16-B aligned load
 
   __device__ __forceinline__ int64_t off(int i) const {
     if (!MERGE) return i;
@@ -54,11 +67,59 @@ struct TkList {
   __device__ __forceinline__ float score(int i) const { return __ldg(sc + off(i)); }
   __device__ __forceinline__ int gid(int i) const {
     if (MERGE) return __ldg(id + off(i));
+    if (I == 1) return i * D + s;
     return (i / I) * I * D + s * I + i % I;  // local slot i of shard s (< 2^31, host-checked)
   }
   __device__ __forceinline__ uint32_t key(int i) const {
     if (MERGE && gid(i) < 0) return 0u;
     return score_key(score(i));
+  }
+  // scores (and merge: ids) of entries i .. i+3 (i a multiple of 4); past the end: -inf
+  __device__ __forceinline__ void raw4(int i, float4& v, int4& t) const {
+    if (vec && i + 3 < n) {
+      const int64_t o = off(i);  // a multiple of 4 entries, all four in one list
+      v = __ldg(reinterpret_cast<const float4*>(sc + o));
+      if (MERGE) t = __ldg(reinterpret_cast<const int4*>(id + o));
+      return;
+    }
+    v.x = i < n ? score(i) : -INFINITY;
+    v.y = i + 1 < n ? score(i + 1) : -INFINITY;
+    v.z = i + 2 < n ? score(i + 2) : -INFINITY;
+    v.w = i + 3 < n ? score(i + 3) : -INFINITY;
+    if (MERGE) {
+      t.x = i < n ? gid(i) : -1;
+      t.y = i + 1 < n ? gid(i + 1) : -1;
+      t.z = i + 2 < n ? gid(i + 2) : -1;
+      t.w = i + 3 < n ? gid(i + 3) : -1;
+    }
+  }
+  __device__ __forceinline__ uint4 keys_of(const float4& v, const int4& t) const {
+    uint4 k = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+    if (MERGE) {
+      k.x = t.x < 0 ? 0u : k.x;
+      k.y = t.y < 0 ? 0u : k.y;
+      k.z = t.z < 0 ? 0u : k.z;
+      k.w = t.w < 0 ? 0u : k.w;
+    }
+    return k;
+  }
+  // keys of entries i .. i+3 (i a multiple of 4); 0 past the end
+  __device__ __forceinline__ uint4 key4(int i) const {
+    if (vec && i + 3 < n) {
+      const int64_t o = off(i);  // a multiple of 4 entries, all four in one list
+      const float4 v = __ldg(reinterpret_cast<const float4*>(sc + o));
+      uint4 k = make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+      if (MERGE) {
+        const int4 t = __ldg(reinterpret_cast<const int4*>(id + o));
+        k.x = t.x < 0 ? 0u : k.x;
+        k.y = t.y < 0 ? 0u : k.y;
+        k.z = t.z < 0 ? 0u : k.z;
+        k.w = t.w < 0 ? 0u : k.w;
+      }
+      return k;
+    }
+    return make_uint4(i < n ? key(i) : 0u, i + 1 < n ? key(i + 1) : 0u,
+                      i + 2 < n ? key(i + 2) : 0u, i + 3 < n ? key(i + 3) : 0u);
   }
 };
 
@@ -87,20 +148,27 @@ __device__ __forceinline__ uint32_t tk_scan(uint32_t v, uint32_t* ws, uint32_t* 
 }
 
 struct TkShared {
-  uint32_t ws[2][kTkWarps];
-  uint32_t bin, above;
+  uint32_t ws[kTkWarps];
+  uint32_t cw[kTkBlockRounds][kTkWarps];   // selected entries per (round, warp) of a block
+  uint32_t off[kTkBlockRounds][kTkWarps];  // their output offsets
+  uint32_t bin, above, base;
+  int run[DCP_MAX_SHARDS + 1];  // merge: first selected entry of each shard's list
 };
 
 // The bin (of nb) holding the krem-th largest in-play key, counting from the top bin, and
 // the number of in-play keys in the bins above it.
-__device__ __forceinline__ void tk_find_bin(const uint32_t* hist, int nb, uint32_t krem,
-                                            TkShared& sh) {
+__device__ __forceinline__ uint32_t tk_find_bin(const uint32_t* hist, int nb, uint32_t krem,
+                                                TkShared& sh) {
   const int bpt = nb / kTkThreads;  // bins per thread, taken from the top
   const int top = nb - 1 - threadIdx.x * bpt;
+  if (threadIdx.x == 0) {  // (a bin is always found: krem never exceeds the keys in play)
+    sh.bin = 0u;
+    sh.above = 0u;
+  }
   uint32_t mine = 0;
   for (int j = 0; j < bpt; ++j) mine += hist[top - j];
   uint32_t tot;
-  uint32_t cum = tk_scan(mine, sh.ws[0], &tot);
+  uint32_t cum = tk_scan(mine, sh.ws, &tot);
   for (int j = 0; j < bpt; ++j) {
     const uint32_t h = hist[top - j];
     if (cum < krem && cum + h >= krem) {
@@ -110,6 +178,12 @@ __device__ __forceinline__ void tk_find_bin(const uint32_t* hist, int nb, uint32
     cum += h;
   }
   __syncthreads();
+  return tot;  // keys in play
+}
+
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t h, uint32_t msk, uint32_t pre,
+                                         int shift, int nb) {
+  if (h != 0u && (h & msk) == pre) atomicAdd(&hist[(h >> shift) & (nb - 1)], 1u);
 }
 
 template <bool MERGE>
@@ -119,51 +193,65 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
   uint32_t* keys = tk_smem + kTkBins;                          // p.stage entries
   int32_t* sorted = reinterpret_cast<int32_t*>(keys + p.stage);  // merge: p.kp entries
   __shared__ TkShared sh;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t li = blockIdx.x;
 
   TkList<MERGE> src;
-  int n;
+  src.vec = p.vec != 0;
   if (MERGE) {
     src.sc = p.score + li * (int64_t)p.stride;
     src.id = p.ids + li * (int64_t)p.stride;
     src.dstride = p.rows * (int64_t)p.stride;
     src.kin = p.stride;
-    n = p.D * p.stride;
+    src.n = p.D * p.stride;
   } else {
     const int o = (int)(li / p.rows);
     src.sc = p.score + li * (int64_t)p.stride;
     src.D = p.D;
     src.I = p.I;
     src.s = p.shard < 0 ? o : p.shard;
-    n = min(max(__ldg(p.len + li), 0), p.stride);
+    src.n = min(max(__ldg(p.len + li), 0), p.stride);
   }
+  const int n = src.n;
   const bool staged = n <= p.stage;
+  const int rounds = (n + kTkRound - 1) / kTkRound;
+  // keys of this thread's four entries of round c
+  auto get4 = [&](int c) -> uint4 {
+    const int i = c * kTkRound + 4 * tid;
+    return staged ? *reinterpret_cast<const uint4*>(keys + i) : src.key4(i);
+  };
 
-  // pass 0: stage the high words, count the valid entries, histogram of the first digit
+  // pass 0: stage the keys, count the valid entries, histogram of the first digit
   for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
   __syncthreads();
-  uint32_t nv = 0;
-  for (int i0 = 0; i0 < n; i0 += 4 * kTkThreads) {
-    uint32_t h[4];
+  for (int c0 = 0; c0 < rounds; c0 += kTkLoadRounds) {
+    // every load of kTkLoadRounds rounds in flight before any is used
+    float4 v[kTkLoadRounds];
+    int4 t[kTkLoadRounds];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * kTkThreads + tid;
-      h[u] = i < n ? src.key(i) : 0u;
+    for (int u = 0; u < kTkLoadRounds; ++u) {
+      if (c0 + u < rounds) {
+        src.raw4((c0 + u) * kTkRound + 4 * tid, v[u], t[u]);
+      } else {
+        v[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        t[u] = make_int4(-1, -1, -1, -1);
+      }
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * kTkThreads + tid;
-      if (staged && i < n) keys[i] = h[u];
-      if (h[u]) {
-        ++nv;
-        atomicAdd(&hist[h[u] >> 21], 1u);
-      }
+    for (int u = 0; u < kTkLoadRounds; ++u) {
+      // (entries of rounds past the end were loaded as -inf: key 0, nothing counted)
+      const uint4 k4 = src.keys_of(v[u], t[u]);
+      if (staged && c0 + u < rounds)  // the staging is a whole number of rounds
+        *reinterpret_cast<uint4*>(keys + (c0 + u) * kTkRound + 4 * tid) = k4;
+      hist_add(hist, k4.x, 0u, 0u, 21, kTkBins);
+      hist_add(hist, k4.y, 0u, 0u, 21, kTkBins);
+      hist_add(hist, k4.z, 0u, 0u, 21, kTkBins);
+      hist_add(hist, k4.w, 0u, 0u, 21, kTkBins);
     }
   }
   __syncthreads();
-  uint32_t nvalid;
-  tk_scan(nv, sh.ws[0], &nvalid);
+  // the first digit's bin; the histogram's total is the number of valid entries
+  const uint32_t nvalid = tk_find_bin(hist, kTkBins, (uint32_t)p.k, sh);
 
   // radix search for the k-th largest key T; the selection is then key >= T
   uint32_t t_hi = 1u, t_lo = 0u;  // fewer valid entries than k: all of them
@@ -176,19 +264,22 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
       if (dg > 0) {
         for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
         __syncthreads();
-        for (int i = tid; i < n; i += kTkThreads) {
-          const uint32_t h = staged ? keys[i] : src.key(i);
-          if (h == 0u) continue;
-          if (!lo) {
-            if ((h & msk_hi) == pre_hi) atomicAdd(&hist[(h >> shift) & (nb - 1)], 1u);
-          } else if (h == pre_hi) {
-            const uint32_t l = ~(uint32_t)src.gid(i);
-            if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
+        for (int c = 0; c < rounds; ++c) {
+          const uint4 k4 = get4(c);
+          const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (!lo) {
+              hist_add(hist, h[e], msk_hi, pre_hi, shift, nb);
+            } else if (h[e] != 0u && h[e] == pre_hi) {
+              const uint32_t l = ~(uint32_t)src.gid(c * kTkRound + 4 * tid + e);
+              if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
+            }
           }
         }
         __syncthreads();
       }
-      tk_find_bin(hist, nb, krem, sh);
+      if (dg > 0) tk_find_bin(hist, nb, krem, sh);
       const uint32_t b = sh.bin;
       krem -= sh.above;
       const uint32_t hb = hist[b];
@@ -206,86 +297,165 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
     t_lo = pre_lo;
   }
 
-  // stable compaction of the selected entries in index order, at most k
-  uint32_t base = 0;
-  int rnd = 0;
-  for (int i0 = 0; i0 < n; i0 += 4 * kTkThreads, ++rnd) {
-    bool sel[4];
-    uint32_t c = 0;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + 4 * tid + u;
-      bool s = false;
-      if (i < n) {
-        const uint32_t h = staged ? keys[i] : src.key(i);
-        s = h != 0u && (h > t_hi || (h == t_hi && (t_lo == 0u || ~(uint32_t)src.gid(i) >= t_lo)));
-      }
-      sel[u] = s;
-      c += s;
+  // stable compaction of the selected entries in index order (at most k), a block of
+  // kTkBlockRounds rounds at a time: count per (round, warp), one scan, then each warp
+  // writes its entries at positions found with ballots
+  auto selected = [&](uint32_t h, int i) -> bool {
+    return h != 0u && (h > t_hi || (h == t_hi && (t_lo == 0u || ~(uint32_t)src.gid(i) >= t_lo)));
+  };
+  const bool no_ties = t_lo == 0u;  // then the selection is key >= t_hi (t_hi >= 1)
+  auto sel4 = [&](const uint4& k4, int i) -> uint32_t {  // bit e: entry i + e is selected
+    if (no_ties)
+      return (uint32_t)(k4.x >= t_hi) | (uint32_t)(k4.y >= t_hi) << 1 |
+             (uint32_t)(k4.z >= t_hi) << 2 | (uint32_t)(k4.w >= t_hi) << 3;
+    return (uint32_t)selected(k4.x, i) | (uint32_t)selected(k4.y, i + 1) << 1 |
+           (uint32_t)selected(k4.z, i + 2) << 2 | (uint32_t)selected(k4.w, i + 3) << 3;
+  };
+  if (tid == 0) sh.base = 0u;
+  for (int c0 = 0; c0 < rounds; c0 += kTkBlockRounds) {
+    const int nr = min(kTkBlockRounds, rounds - c0);
+    uint32_t selmask = 0;  // 4 bits per round of the block
+    for (int cr = 0; cr < nr; ++cr) {
+      const int c = c0 + cr;
+      const uint32_t m4 = sel4(get4(c), c * kTkRound + 4 * tid);
+      selmask |= m4 << (4 * cr);
+      const uint32_t wsum = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(m4));
+      if (lane == 0) sh.cw[cr][warp] = wsum;
     }
-    // exclusive prefix over threads (one barrier per round: warp totals double-buffered)
-    const int lane = tid & 31, warp = tid >> 5;
-    uint32_t x = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    uint32_t* ws = sh.ws[rnd & 1];
-    if (lane == 31) ws[warp] = x;
     __syncthreads();
-    uint32_t before = 0, tot = 0;
+    if (warp == 0) {  // exclusive scan of the block's (round, warp) counts in index order
+      const int per = kTkBlockRounds * kTkWarps / 32;
+      uint32_t v[kTkBlockRounds * kTkWarps / 32], run = 0;
 #pragma unroll
-    for (int w = 0; w < kTkWarps; ++w) {
-      const uint32_t t = ws[w];
-      if (w < warp) before += t;
-      tot += t;
-    }
-    uint32_t pos = base + before + x - c;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (sel[u] && pos < (uint32_t)p.k) {
-        const int i = i0 + 4 * tid + u;
-        if (MERGE) {
-          sorted[pos] = src.gid(i);
-        } else {
-          p.cand_score[li * p.k + pos] = src.score(i);
-          p.cand_idx[li * p.k + pos] = src.gid(i);
-        }
+      for (int j = 0; j < per; ++j) {
+        const int q = lane * per + j;
+        v[j] = q / kTkWarps < nr ? sh.cw[q / kTkWarps][q % kTkWarps] : 0u;
+        run += v[j];
       }
-      pos += sel[u];
+      uint32_t x = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      uint32_t pos = sh.base + x - run;
+#pragma unroll
+      for (int j = 0; j < per; ++j) {
+        const int q = lane * per + j;
+        sh.off[q / kTkWarps][q % kTkWarps] = pos;
+        pos += v[j];
+      }
+      const uint32_t total = __shfl_sync(0xffffffffu, x, 31);
+      __syncwarp();
+      if (lane == 0) sh.base += total;
     }
-    base += tot;
+    __syncthreads();
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int cr = 0; cr < nr; ++cr) {
+      const int c = c0 + cr;
+      const uint32_t m4 = (selmask >> (4 * cr)) & 15u;
+      // entries of lower lanes come first, then this lane's in order
+      uint32_t pos = sh.off[cr][warp];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pos += __popc(__ballot_sync(0xffffffffu, (m4 >> e) & 1u) & lt);
+      if (m4 == 0u) continue;
+      const int i = c * kTkRound + 4 * tid;
+      uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
+      if (!MERGE) k4 = get4(c);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (((m4 >> e) & 1u) && pos < (uint32_t)p.k) {
+          if (MERGE) {
+            sorted[pos] = i + e;  // the entry; its id is loaded below, all at once
+          } else {
+            // the score from its key (exact; a zero is re-read, the key merges -0 and +0)
+            const uint32_t h = e == 0 ? k4.x : e == 1 ? k4.y : e == 2 ? k4.z : k4.w;
+            p.cand_score[li * p.k + pos] = h == 0x80000000u ? src.score(i + e) : key_score(h);
+            p.cand_idx[li * p.k + pos] = src.gid(i + e);
+          }
+        }
+        pos += (m4 >> e) & 1u;
+      }
+    }
+    __syncthreads();  // the offsets are read before the next block rewrites them
   }
-  const int cnt = (int)min(base, (uint32_t)p.k);
+  const int cnt = (int)min(sh.base, (uint32_t)p.k);
 
-  if (!MERGE) {
+  if constexpr (!MERGE) {
     for (int j = cnt + tid; j < p.k; j += kTkThreads) {
       p.cand_score[li * p.k + j] = -INFINITY;
       p.cand_idx[li * p.k + j] = -1;
     }
-    return;
-  }
-  // merge: the selected ids in increasing order (bitonic sort over p.kp >= k entries)
-  __syncthreads();
-  for (int j = cnt + tid; j < p.kp; j += kTkThreads) sorted[j] = INT_MAX;
-  __syncthreads();
-  for (int size = 2; size <= p.kp; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = tid; t < p.kp / 2; t += kTkThreads) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const int a = sorted[i], b = sorted[j];
-        if ((a > b) == ((i & size) == 0)) {
-          sorted[i] = b;
-          sorted[j] = a;
+  } else {
+    // sorted[0, cnt) holds the selected entries in index order: shard d's list is the run
+    // of entries in [d * kin, (d + 1) * kin).  First the run boundaries, then the ids.
+    if (tid <= p.D) {
+      const int target = tid * p.stride;
+      int lo = 0, hi = cnt;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sorted[mid] < target) lo = mid + 1; else hi = mid;
+      }
+      sh.run[tid] = lo;
+    }
+    __syncthreads();
+    for (int j = tid; j < cnt; j += kTkThreads) sorted[j] = src.gid(sorted[j]);
+    __syncthreads();
+    // runs in increasing id order (as dcp_topk_local writes its lists): place every id by
+    // its rank -- its place in its own run plus the smaller ids of the other runs
+    bool unsorted = false;  // a pair inside a run out of order (pairs across runs may descend)
+    for (int j = tid; j + 1 < cnt; j += kTkThreads) {
+      int lo = 0, hi = p.D;  // the run of entry j + 1: the last d with run[d] <= j + 1
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sh.run[mid] <= j + 1) lo = mid; else hi = mid - 1;
+      }
+      unsorted |= sh.run[lo] != j + 1 && sorted[j] >= sorted[j + 1];
+    }
+    int32_t* out = p.topk + li * p.k;
+    if (!__syncthreads_or(unsorted)) {
+      for (int j = tid; j < cnt; j += kTkThreads) {
+        const int x = sorted[j];
+        int lo = 0, hi = p.D - 1;  // the run of entry j
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (sh.run[mid] <= j) lo = mid; else hi = mid - 1;
+        }
+        int pos = j - sh.run[lo];
+        for (int d = 0; d < p.D; ++d) {
+          if (d == lo) continue;
+          int a = sh.run[d], b = sh.run[d + 1];  // smaller ids of run d
+          while (a < b) {
+            const int mid = (a + b) >> 1;
+            if (sorted[mid] < x) a = mid + 1; else b = mid;
+          }
+          pos += a - sh.run[d];
+        }
+        out[pos] = x;
+      }
+      for (int j = cnt + tid; j < p.k; j += kTkThreads) out[j] = -1;
+    } else {
+      // any order: bitonic sort over p.kp >= k entries
+      for (int j = cnt + tid; j < p.kp; j += kTkThreads) sorted[j] = INT_MAX;
+      __syncthreads();
+      for (int size = 2; size <= p.kp; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int t = tid; t < p.kp / 2; t += kTkThreads) {
+            const int i = 2 * t - (t & (stride - 1));
+            const int j = i + stride;
+            const int a = sorted[i], b = sorted[j];
+            if ((a > b) == ((i & size) == 0)) {
+              sorted[i] = b;
+              sorted[j] = a;
+            }
+          }
+          __syncthreads();
         }
       }
-      __syncthreads();
+      for (int j = tid; j < p.k; j += kTkThreads) out[j] = j < cnt ? sorted[j] : -1;
     }
+    if (tid == 0 && p.count) p.count[li] = cnt;
   }
-  for (int j = tid; j < p.k; j += kTkThreads) p.topk[li * p.k + j] = j < cnt ? sorted[j] : -1;
-  if (tid == 0 && p.count) p.count[li] = cnt;
 }
 
 namespace {
@@ -294,25 +464,38 @@ size_t tk_smem_bytes(int stage, int kp) { return (size_t)(kTkBins + stage + kp) 
 template <bool MERGE>
 cudaError_t tk_launch(const TopkParams& p, int64_t lists, cudaStream_t st) {
   const size_t smem = tk_smem_bytes(p.stage, MERGE ? p.kp : 0);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel<MERGE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // raise the kernel's dynamic shared-memory limit once per device and size
+  static int allowed[kTkMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kTkMaxDevices || (size_t)allowed[dev] < smem) {
+    e = cudaFuncSetAttribute(topk_kernel<MERGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kTkMaxDevices) allowed[dev] = (int)smem;
+  }
   topk_kernel<MERGE><<<(unsigned)lists, kTkThreads, smem, st>>>(p);
   return cudaGetLastError();
 }
 }  // namespace
 
+// entries staged per list: the longest list, at most kTkStageMax, in whole rounds
+int tk_stage(int64_t n_max) {
+  const int64_t s = n_max < kTkStageMax ? n_max : kTkStageMax;
+  return (int)((s + kTkRound - 1) / kTkRound * kTkRound);
+}
+
 cudaError_t launch_topk_local(TopkParams p, int n_in, cudaStream_t st) {
   if (p.rows == 0) return cudaSuccess;
-  p.stage = p.stride < kTkStageMax ? p.stride : kTkStageMax;
+  p.stage = tk_stage(p.stride);
   p.kp = 0;
   return tk_launch<false>(p, p.rows * n_in, st);
 }
 
 cudaError_t launch_topk_merge(TopkParams p, cudaStream_t st) {
   if (p.rows == 0) return cudaSuccess;
-  const int64_t n = (int64_t)p.D * p.stride;
-  p.stage = n < kTkStageMax ? (int)n : kTkStageMax;
+  p.stage = tk_stage((int64_t)p.D * p.stride);
   int kp = 1;
   while (kp < p.k) kp <<= 1;
   p.kp = kp;

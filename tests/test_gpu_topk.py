@@ -116,6 +116,23 @@ def test_merge_matches_oracle(dcp, D, kin, k):
     assert np.array_equal(cnt.cpu().numpy(), wc)
 
 
+@pytest.mark.parametrize("D,kin,k", [(2, 50, 64), (8, 2048, 2048), (64, 20, 300), (1, 300, 100),
+                                     (5, 100, 7), (8, 4096, 4096)])
+def test_merge_of_ascending_lists_matches_oracle(dcp, D, kin, k):
+    """Lists in increasing id order, as dcp_topk_local writes them (the merge then places
+    every id by rank; other lists are sorted)."""
+    R = 6
+    cs, ci = _random_candidates(D, R, kin, seed=D * 17 + k)
+    order = np.argsort(ci.numpy(), axis=2, kind="stable")
+    ci = torch.from_numpy(np.take_along_axis(ci.numpy(), order, 2).copy())
+    cs = torch.from_numpy(np.take_along_axis(cs.numpy(), order, 2).copy())
+    top, cnt = dcp.dcp_topk_merge(cs.to(dev), ci.to(dev), k)
+    torch.cuda.synchronize()
+    wt, wc = otk.merge_topk(cs.numpy(), ci.numpy(), k)
+    assert np.array_equal(top.cpu().numpy(), wt)
+    assert np.array_equal(cnt.cpu().numpy(), wc)
+
+
 def test_merge_max_topk(dcp):
     k = 16384
     cs, ci = _random_candidates(2, 2, k, seed=77, pad=0.3)
