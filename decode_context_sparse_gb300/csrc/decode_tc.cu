@@ -71,16 +71,16 @@ struct TcCfg;
 // gather lands on a 128-B aligned stride.
 template <>
 struct TcCfg<DCP_KV_FP8_E4M3_S128> {
-  static constexpr int NACC = 2, NS = 2, NK = 4, NP = 1, NSB = 2;
+  static constexpr int NACC = 2, NS = 2, NK = 4, NP = 2, NSB = 1;
   static constexpr int LAT_TOK = 256, TAIL_TOK = 144, TAIL_GSTRIDE = 640;
 };
 template <>
 struct TcCfg<DCP_KV_BF16> {
-  static constexpr int NACC = 1, NS = 2, NK = 4, NP = 1, NSB = 2;
+  static constexpr int NACC = 1, NS = 2, NK = 4, NP = 2, NSB = 1;
   static constexpr int LAT_TOK = 512, TAIL_TOK = 64, TAIL_GSTRIDE = 256;
 };
 
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 640;
 constexpr int kColO = 0, kColQ = 256, kColS = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kScaleFloor = 8.67361737988403547e-19f;  // 2^-60
@@ -126,6 +126,9 @@ struct TcShared {
   uint64_t s_full[2], p_full[2], pv_done[2], q_ready, in_full[2], out_free[2], drain;
   uint64_t self_full[2], self_free[2];  // stage A -> stage B hand-over of this CTA's partial
   uint64_t s_free[2];                   // stage A has read a logit buffer out of TMEM
+  uint64_t bx_full[4][2], bl_full[4];   // stage B pairs: partial row maxima / row sums posted
+  float bx[2][2][128];                  // [half][tile parity][head] partial row max of a tile
+  float bl[2][128];                     // [half][head] partial row sum of a unit
   uint32_t stg_mask[4];
   uint32_t kt_mask[8];        // valid-slot mask of each K tile
   uint32_t stg_issued[4];     // gathers issued per staging slot (for the teardown wait)
@@ -253,9 +256,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.p_full[i], 4);
+      mbar_init(&sh.p_full[i], 8);
       mbar_init(&sh.in_full[i], 1);
-      mbar_init(&sh.out_free[i], 4);  // one arrival per softmax warp of the peer
+      mbar_init(&sh.out_free[i], 8);  // one arrival per stage-B warp of the peer
       mbar_init(&sh.s_free[i], 4);
     }
     mbar_init(&sh.pv_done[0], 1);
@@ -264,7 +267,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     mbar_init(&sh.drain, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.self_full[i], 4);
-      mbar_init(&sh.self_free[i], 4);
+      mbar_init(&sh.self_free[i], 8);
+    }
+    for (int g = 0; g < 4; ++g) {
+      mbar_init(&sh.bx_full[g][0], 2);
+      mbar_init(&sh.bx_full[g][1], 2);
+      mbar_init(&sh.bl_full[g], 2);
     }
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -659,7 +667,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         mbar_arrive(&sh.stg_empty[slot]);
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 12 && warp < 16) {
     // ============================================================ softmax stage A
     const int h = tid - 384;  // head = TMEM lane
     const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
@@ -772,13 +780,21 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     __syncwarp();
   } else if (warp >= 8) {
     // ============================================================ softmax stage B / epilogue
-    const int h = tid - 256;  // head = TMEM lane
-    const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
+    // Warps 8-11 and 16-19: warp 8+g and warp 16+g share heads 32g .. 32g+31 (TMEM lanes of
+    // sub-partition g); half 0 takes columns 0-15 of every tile and O columns 0-127, half 1
+    // columns 16-31 and O columns 128-255.  The two exchange their partial row maxima every
+    // tile and their partial row sums at the end of a unit (bounded mbarrier waits).
+    constexpr int TH = TN / 2;
+    const int half = warp >= 16 ? 1 : 0;
+    const int grp = warp & 3;
+    const int h = grp * 32 + lane;  // head = TMEM lane
+    const int cb = half * TH;       // first column of this half
+    const uint32_t trow = tbase + ((uint32_t)(grp * 32) << 16);
     const float* xin = reinterpret_cast<const float*>(smem + L::OFF_X);
     const float* xself = reinterpret_cast<const float*>(smem + L::OFF_SELF);
 
     // units without any slot: zero output, -inf LSE
-    if (!(FUSED && SPARSE)) {
+    if (!(FUSED && SPARSE) && half == 0) {
       for (int64_t u = pair; u < U; u += P) {
         const UnitInfo x = get_unit<FUSED, SPARSE>(p, u);
         if (x.ntile != 0 || h >= H) continue;
@@ -796,24 +812,32 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
 
     Walk<FUSED, SPARSE> w;
     w.init(p, sh.unit0, sh.tile0, ntiles);
-    float m_ref = -INFINITY, lsum = 0.f;
+    float m_ref = -INFINITY, lsum = 0.f;  // lsum: this half's share of the row sum
     int64_t U0 = t0 - sh.tile0;   // global index of the current unit's first tile
     bool from_start = sh.tile0 == 0;
     int slot_idx = 0;             // workspace slot of a split unit: 0 first unit, 1 last
+    int nunit = 0;                // units finished (parity of the row-sum exchange)
     bool ok = true;
 
-    // Finish the current unit: normalise and write O (or a split partial) and the LSE.
+    // Finish the current unit: normalise and write this half's O columns (or a split
+    // partial) and the LSE.
     auto finish_unit = [&](int jl, bool complete) {
+      sh.bl[half][h] = lsum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.bl_full[grp]);
+      if (!(ok = mbar_wait(&sh.bl_full[grp], nunit & 1, abort_flag))) return;
+      ++nunit;
+      const float ltot = lsum + sh.bl[half ^ 1][h];
       volatile int no_abort = 0;
       mbar_wait(&sh.pv_done[jl & 1], (jl >> 1) & 1, ok ? abort_flag : &no_abort);
       tc_fence_after();
-      const float fix = lsum > 0.f ? 1.0f / lsum : 0.f;
-      const float lse_v = lsum > 0.f ? (m_ref + __log2f(lsum)) * kLn2 : -INFINITY;
+      const float fix = ltot > 0.f ? 1.0f / ltot : 0.f;
+      const float lse_v = ltot > 0.f ? (m_ref + __log2f(ltot)) * kLn2 : -INFINITY;
       const int64_t u = w.u;
       const int64_t oi = (u * H + h) * kDv + crank * 256;
       float* wso = p.tc_o + (((int64_t)pair * 2 + slot_idx) * 128 + h) * kDv + crank * 256;
-      // four 16-column chunks per TMEM wait
-      for (int c4 = 0; c4 < 16; c4 += 4) {
+      // this half's eight 16-column chunks, four per TMEM wait
+      for (int c4 = half * 8; c4 < half * 8 + 8; c4 += 4) {
         uint32_t v[4][16];
 #pragma unroll
         for (int k = 0; k < 4; ++k) tmem_ld16(trow + kColO + 16 * (c4 + k), v[k]);
@@ -848,13 +872,13 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       }
       tc_fence_before();
       if (complete) {
-        if (crank == 0 && h < H) p.lse[u * H + h] = lse_v;
+        if (half == 0 && crank == 0 && h < H) p.lse[u * H + h] = lse_v;
         return;
       }
       // split unit: publish this pair's partial and its descriptor; the split-merge kernel
       // that follows on the stream combines the parts of every split unit
-      __stcg(p.tc_l + (((int64_t)pair * 2 + slot_idx) * 2 + crank) * 128 + h, lse_v);
-      if (crank == 0 && h == 0) {
+      if (half == 0) __stcg(p.tc_l + (((int64_t)pair * 2 + slot_idx) * 2 + crank) * 128 + h, lse_v);
+      if (half == 0 && crank == 0 && h == 0) {
         int64_t* d = p.tc_desc + 2 + ((int64_t)pair * 2 + slot_idx) * 3;
         d[0] = u;
         d[1] = U0;
@@ -868,14 +892,14 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
       // P(j) goes into shared-memory buffer j % NP once P.V(j-NP) has read it (waited below)
       unsigned char* prow = smem + L::OFF_P + (j % C::NP) * L::P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
-      float s[TN];
+      float s[TH];
       // A(j) hands over after it saw the K tile complete: the tile's metadata is valid
       const int xs = j % C::NSB;
       if (!(ok = mbar_wait(&sh.self_full[xs], (j / C::NSB) & 1, abort_flag))) break;
-      const uint32_t mask = sh.kt_mask[j % NK];
-      const float* srow = xself + (xs * 128 + h) * L::XSTRIDE;
+      const uint32_t mask = sh.kt_mask[j % NK] >> cb;
+      const float* srow = xself + (xs * 128 + h) * L::XSTRIDE + cb;
 #pragma unroll
-      for (int c = 0; c < TN / 4; ++c) {
+      for (int c = 0; c < TH / 4; ++c) {
         const float4 v = *reinterpret_cast<const float4*>(srow + 4 * c);
         s[4 * c] = v.x;
         s[4 * c + 1] = v.y;
@@ -885,9 +909,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.self_free[xs]);
       if (!(ok = mbar_wait(&sh.in_full[x], (j >> 1) & 1, abort_flag, true))) break;
-      const float* xrow = xin + (x * 128 + h) * L::XSTRIDE;
+      const float* xrow = xin + (x * 128 + h) * L::XSTRIDE + cb;
 #pragma unroll
-      for (int c = 0; c < TN / 4; ++c) {
+      for (int c = 0; c < TH / 4; ++c) {
         const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * c);
         s[4 * c] += v.x;
         s[4 * c + 1] += v.y;
@@ -898,37 +922,43 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       // hands its rows back to the peer at the end of this stage
       if (warp == 8 && lane == 0) mbar_arrive_expect_tx(&sh.in_full[x], L::X_BYTES);
       // online softmax (base 2) with a lazily raised reference
-      if (mask != 0xffffffffu) {
+      if ((mask & 0xffffu) != 0xffffu) {
 #pragma unroll
-        for (int t = 0; t < TN; ++t)
+        for (int t = 0; t < TH; ++t)
           if (!((mask >> t) & 1)) s[t] = -INFINITY;
       }
-      float mt;
+      float mh;
       {
-        float r[TN / 2];
+        float r[TH / 2];
 #pragma unroll
-        for (int t = 0; t < TN / 2; ++t) r[t] = fmaxf(s[t], s[t + TN / 2]);
+        for (int t = 0; t < TH / 2; ++t) r[t] = fmaxf(s[t], s[t + TH / 2]);
 #pragma unroll
-        for (int w2 = TN / 4; w2 >= 1; w2 >>= 1)
+        for (int w2 = TH / 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
           for (int t = 0; t < w2; ++t) r[t] = fmaxf(r[t], r[t + w2]);
-        mt = r[0];
+        mh = r[0];
       }
       // every inbox value of this warp has been loaded and used (the max depends on all of
       // them): hand the rows back to the peer now; a relaxed arrive suffices
-      asm volatile("" ::"f"(mt) : "memory");
+      asm volatile("" ::"f"(mh) : "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster_relaxed(&sh.out_free[x], peer);
+      // the row max of the whole tile: the two halves post theirs and read the other's
+      sh.bx[half][x][h] = mh;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.bx_full[grp][x]);
+      if (!(ok = mbar_wait(&sh.bx_full[grp][x], (j >> 1) & 1, abort_flag))) break;
+      const float mt = fmaxf(mh, sh.bx[half ^ 1][x][h]);
       // per head: raise the reference when the tile max exceeds it by more than 2^8; the
       // TMEM read-modify-write of O is warp-collective, so a warp rescales when any of its
-      // heads needs it (alpha = 1 for the others)
+      // heads needs it (alpha = 1 for the others); each half rescales its own O columns
       float alpha = 1.0f;
       const bool raise = mt > m_ref + 8.0f;
       if (raise && m_ref != -INFINITY) alpha = fast_exp2(m_ref - mt);
       if (__any_sync(0xffffffffu, alpha != 1.0f)) {
         if (!(ok = mbar_wait(&sh.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        for (int c = 0; c < 16; ++c) {
+        for (int c = half * 8; c < half * 8 + 8; ++c) {
           uint32_t v[16];
           tmem_ld16(trow + kColO + 16 * c, v);
           tmem_ld_wait();
@@ -941,16 +971,16 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         lsum *= alpha;
         m_ref = mt;
       }
-      float pr[TN];
+      float pr[TH];
       {
         const float mr = m_ref == -INFINITY ? 0.f : m_ref;  // all -inf: every p is 0
 #pragma unroll
-        for (int t = 0; t < TN; ++t) pr[t] = fast_exp2(s[t] - mr);
-        float r[TN / 2];
+        for (int t = 0; t < TH; ++t) pr[t] = fast_exp2(s[t] - mr);
+        float r[TH / 2];
 #pragma unroll
-        for (int t = 0; t < TN / 2; ++t) r[t] = pr[t] + pr[t + TN / 2];
+        for (int t = 0; t < TH / 2; ++t) r[t] = pr[t] + pr[t + TH / 2];
 #pragma unroll
-        for (int w2 = TN / 4; w2 >= 1; w2 >>= 1)
+        for (int w2 = TH / 4; w2 >= 1; w2 >>= 1)
 #pragma unroll
           for (int t = 0; t < w2; ++t) r[t] += r[t + w2];
         lsum += r[0];
@@ -959,20 +989,20 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           !(ok = mbar_wait(&sh.pv_done[(j - C::NP) & 1], ((j - C::NP) >> 1) & 1, abort_flag)))
         break;
       const int sw = h & 7;  // SW128: 16-B chunk c of row h sits at chunk c ^ (h & 7)
-      if (!FP8) {
-        uint32_t pw[TN / 2];
+      if (!FP8) {  // P row: 32 bf16 in chunks 0-3; this half's 16 in chunks 2*half, 2*half+1
+        uint32_t pw[TH / 2];
 #pragma unroll
-        for (int i = 0; i < TN / 2; ++i) pw[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+        for (int i = 0; i < TH / 2; ++i) pw[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
+        for (int c = 0; c < 2; ++c)
+          *reinterpret_cast<uint4*>(prow + (((2 * half + c) ^ sw) << 4)) =
               make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      } else {
-        const uint4* pl4 = reinterpret_cast<const uint4*>(meta + 8 * TN);   // bf16 s_lo x 32
-        const uint4* ph4 = pl4 + TN / 8;                                     // bf16 s_hi x 32
-        uint32_t plo[TN / 2], phi[TN / 2];
+      } else {  // P row: [p*s_lo slots 0-31 | p*s_hi slots 0-31], chunks 0-3 | 4-7
+        const uint4* pl4 = reinterpret_cast<const uint4*>(meta + 8 * TN) + 2 * half;  // bf16 s_lo
+        const uint4* ph4 = pl4 + TN / 8;                                             // bf16 s_hi
+        uint32_t plo[TH / 2], phi[TH / 2];
 #pragma unroll
-        for (int i = 0; i < TN / 8; ++i) {
+        for (int i = 0; i < TH / 8; ++i) {
           const uint4 a = pl4[i], b = ph4[i];
           const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
@@ -988,10 +1018,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           }
         }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          *reinterpret_cast<uint4*>(prow + ((c ^ sw) << 4)) =
+        for (int c = 0; c < 2; ++c) {
+          *reinterpret_cast<uint4*>(prow + (((2 * half + c) ^ sw) << 4)) =
               make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
-          *reinterpret_cast<uint4*>(prow + (((4 + c) ^ sw) << 4)) =
+          *reinterpret_cast<uint4*>(prow + (((4 + 2 * half + c) ^ sw) << 4)) =
               make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
         }
       }
@@ -1002,6 +1032,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       if (lane == 0) mbar_arrive(&sh.p_full[j & 1]);
       if (w.last()) {
         finish_unit(j, from_start);
+        if (!ok) break;
         m_ref = -INFINITY;
         lsum = 0.f;
         from_start = true;
