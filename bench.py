@@ -116,7 +116,7 @@ def dist_env():
     return ws, rank, local
 
 
-TRAFFIC_BYTES_PER_ROW = (167.1744e6 + 15.179776e6) / 96
+TRAFFIC_BYTES_PER_ROW = (167.572736e6 + 16.186112e6) / 96
 
 
 def make_workload(dev, seqs=64):
@@ -502,7 +502,7 @@ def main():
         roof = {"bound": "hbm", "achieved": hbm_tbs * 1e3, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_tbs * 1e3 / peaks["hbm_gbs"]}
     # DRAM bytes (read + write) per launch from ncu (profiles/decode_tc_fused_topk2048_fp8_96rows.md:
-    # 167.2 MB + 15.2 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
+    # 167.6 MB + 16.2 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
     roof["traffic"] = TRAFFIC_BYTES_PER_ROW * R if prob.heads == 128 else None
     roof["traffic_unit"] = "bytes"
     roof["peak_src"] = peaks["src"]

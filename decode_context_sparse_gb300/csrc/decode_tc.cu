@@ -13,7 +13,7 @@
 // shared memory (one bulk copy per warp, completing on the peer's mbarrier) and both CTAs
 // run the same softmax.
 //
-// Per CTA (512 threads), tiles of 32 key slots:
+// Per CTA (640 threads), tiles of 32 key slots:
 //   warps 1-3   loaders (tiles round-robin; as many as staging slots, at most three; the
 //               others idle):
 //               slot id -> owner shard / local slot -> page
@@ -27,7 +27,8 @@
 //   warps 12-15 softmax stage A: thread h owns head h (TMEM lane h): reads its logits of
 //               a tile, scales them, hands this CTA's partial to stage B through a local
 //               box in shared memory and copies the box to the peer CTA's inbox; loads Q;
-//   warps 8-11  softmax stage B: adds the two partials, online softmax in base 2 with a
+//   warps 8-11, 16-19  softmax stage B, two warps per group of 32 heads, each on half of
+//               a tile's columns: adds the two partials, online softmax in base 2 with a
 //               lazily raised reference max (the output is rescaled only when the max
 //               grows by more than 2^8), writes P as bf16 into shared memory, and at the
 //               end of a row normalises O and writes it out (or a partial of a split row).
