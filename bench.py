@@ -261,6 +261,54 @@ def time_topk_producer(dcp, dev, peaks, stream, flush, steps):
             "launches_per_call": 2}
 
 
+def time_prefill_chunk(dcp, dev, peaks, stream, flush, steps):
+    """A chunked-prefill step of the same model shapes: 2 sequences x 64 chunk tokens after a
+    16384-token cached prefix, 128 heads, FP8, D = 8.  Timed as the prefix + chunk partials
+    merged by LSE (the composition) and as one fused dense launch over the same lengths.
+    FLOPs: 2*H*(576+512) per (row, visible slot)."""
+    import synth
+    prob = synth.prefill_chunk_fp8(device=dev)
+    chunk = 64
+    prefix, ids = synth.prefill_chunk_inputs(prob, chunk)
+    pmax = int(prefix.max().item())
+    lmax = int(prob.row_len.max().item())
+    out = torch.empty((prob.rows, prob.heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((prob.rows, prob.heads), dtype=torch.float32, device=dev)
+
+    def composed():
+        dcp.mla_prefill_chunk_dcp(prob.q, prob.pool, prob.kv_dtype, prob.block_table, prob.row_seq,
+                                  prob.sm_scale, prob.dcp, prob.interleave, prefix_len=prefix,
+                                  chunk_idx=ids, max_prefix_len=pmax, out=out, lse=lse)
+
+    def fused():
+        dcp.mla_decode_dcp_fused(prob.q, prob.pool, prob.kv_dtype, prob.block_table, prob.row_seq,
+                                 prob.sm_scale, prob.dcp, prob.interleave, kv_len=prob.row_len,
+                                 max_kv_len=lmax, out=out, lse=lse)
+
+    res = {}
+    flops = 2.0 * prob.heads * (D_QK + D_V) * float(prob.row_len.sum().item())
+    for name, f in (("composed", composed), ("fused_dense", fused)):
+        for _ in range(3):
+            f()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(3, steps // 2))]
+        for a, b in evs:
+            flush.fill_(5)
+            a.record(stream)
+            f()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        tf = flops / (ms / 1e3) / 1e12
+        res[name] = {"us": 1e3 * ms, "chunk_tokens_per_s": prob.rows / (ms / 1e3),
+                     "tflops": tf, "frac": tf / peaks["bf16_tflops"]}
+    res["workload"] = ("chunked prefill, 2 seqs x 64 chunk tokens after a 16384-token prefix, "
+                       "128 heads, FP8, DCP=8")
+    res["bound"] = "tensor"
+    res["peak_tflops"] = peaks["bf16_tflops"]
+    return res
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest of every rank's x (x itself without a process group)."""
     import torch.distributed as dist
@@ -445,6 +493,7 @@ def main():
     unfused_ms = statistics.mean(a.elapsed_time(b) for a, b in uev)
     kvw = time_kv_cache_write(dcp, dev, peaks, stream, flush, args.steps)
     topk_prod = time_topk_producer(dcp, dev, peaks, stream, flush, args.steps)
+    prefill = time_prefill_chunk(dcp, dev, peaks, stream, flush, args.steps)
     graph_step = time_graph_step(dcp, dev)
 
     # end to end through the public API with host buffers: H2D of the step's inputs (queries,
@@ -527,6 +576,7 @@ def main():
         "roofline": roof,
         "kv_cache_write": kvw,
         "topk_producer": topk_prod,
+        "prefill_chunk": prefill,
         "graph_step": graph_step,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": h2d,

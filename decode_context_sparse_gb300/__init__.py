@@ -379,6 +379,35 @@ def mla_decode_dcp_fused(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, d
     return out, lse
 
 
+def mla_prefill_chunk_dcp(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, dcp, interleave, *,
+                          prefix_len, chunk_idx, max_prefix_len, out=None, lse=None, stream=None):
+    """Attention of a prefill chunk's query rows under DCP, as partials merged by LSE.
+
+    Row r attends to its sequence's cached prefix, global slots [0, prefix_len[r]) held by the
+    D shards under the owner rule (one dense partial per shard, over that shard's local
+    slots), and to the slots of the chunk it sees, chunk_idx[r] (global ids, -1 padded; one
+    sparse partial per shard after the remap).  The 2*dcp partials are merged with LSE
+    weights.  Steps: dcp_local_lengths, mla_decode_partial_lse (dense), dcp_remap_topk,
+    mla_decode_partial_lse (sparse), dcp_lse_merge.  max_prefix_len bounds prefix_len on
+    the host (no device read).  Returns (out [R, H, 512] bf16, lse [R, H] fp32)."""
+    R, H, _ = q.shape
+    _i32(prefix_len, "prefix_len")
+    _i32(chunk_idx, "chunk_idx")
+    po = torch.empty((2 * dcp, R, H, 512), dtype=torch.float32, device=q.device)
+    pl = torch.empty((2 * dcp, R, H), dtype=torch.float32, device=q.device)
+    # the longest local prefix any shard holds (slot counts of one owner are at most
+    # interleave * ceil(L / (interleave * dcp)))
+    local_max = interleave * -(-int(max_prefix_len) // (interleave * dcp))
+    ll = dcp_local_lengths(prefix_len, dcp, interleave, stream=stream)
+    mla_decode_partial_lse(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, kv_len=ll,
+                           max_kv_len=local_max, num_shards=dcp, out=po[:dcp], lse=pl[:dcp],
+                           stream=stream)
+    loc, cnt = dcp_remap_topk(chunk_idx, dcp, interleave, stream=stream)
+    mla_decode_partial_lse(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx=loc,
+                           count=cnt, num_shards=dcp, out=po[dcp:], lse=pl[dcp:], stream=stream)
+    return dcp_lse_merge(po, pl, out=out, lse=lse, stream=stream)
+
+
 def mla_decode_dcp_fused_noalloc(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, dcp,
                                  interleave, *, out, lse, idx=None, kv_len=None, max_kv_len=None,
                                  num_splits=0, checked=False, err_flag=None, stream=None):

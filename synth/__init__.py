@@ -329,3 +329,36 @@ def topk_producer_topk2048(device="cpu", seqs=64, mtp=6, seq_len=131072, dcp=8, 
     stride = local_len_bound(seq_len, dcp, interleave)
     scores = index_scores(dcp, seqs * mtp, stride, gen)
     return TopkProducerProblem(dcp, interleave, k, row_len, scores, stride)
+
+
+# ---------------------------------------------------------------------------------------
+# Chunked prefill: the query rows of one prefill chunk per sequence.
+# ---------------------------------------------------------------------------------------
+
+def prefill_chunk_problem(name, prefix_lens, chunk, heads, kv_dtype, dcp, interleave=1, seed=7,
+                          device="cpu"):
+    """Sequences of prefix_lens[b] cached tokens followed by a chunk of `chunk` new tokens
+    (all already in the pool); one query row per chunk token, row i of a chunk seeing the
+    prefix and chunk tokens 0..i (a dense problem whose row i sees prefix + i + 1 slots)."""
+    return make_decode_problem(name, [int(p) + chunk for p in prefix_lens], heads, None, kv_dtype,
+                               dcp, interleave, mtp=chunk, seed=seed, device=device)
+
+
+def prefill_chunk_inputs(prob: DecodeProblem, chunk: int):
+    """Per row of a prefill_chunk_problem: the cached-prefix length [R] int32 and the chunk
+    slots the row sees [R, chunk] int32 (global ids prefix .. prefix + i, then -1)."""
+    dev = prob.q.device
+    L = prob.seq_len.to(dev)[prob.row_seq.long()]
+    prefix = (L - chunk).to(torch.int32)
+    i = torch.arange(prob.rows, device=dev) % chunk
+    c = torch.arange(chunk, device=dev)
+    ids = prefix.unsqueeze(1).to(torch.int64) + c.unsqueeze(0)
+    ids = torch.where(c.unsqueeze(0) <= i.unsqueeze(1), ids, torch.full_like(ids, -1))
+    return prefix.contiguous(), ids.to(torch.int32).contiguous()
+
+
+def prefill_chunk_fp8(device="cpu", seqs=2, prefix=16384, chunk=64, heads=128, dcp=8):
+    """A prefill chunk of the top-k 2048 decode model's shapes: 2 sequences x 64 chunk tokens
+    after a 16384-token cached prefix, 128 heads, FP8 KV, D = 8 token-interleaved."""
+    return prefill_chunk_problem("prefill_chunk_fp8", [prefix] * seqs, chunk, heads, KV_FP8, dcp,
+                                 1, seed=7, device=device)
