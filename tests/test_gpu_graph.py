@@ -104,3 +104,52 @@ def test_multi_layer_step_graph_with_shared_remap(dcp):
     torch.cuda.synchronize()
     for (ro, rl), o, l in zip(ref, outs, lses):
         assert torch.equal(o, ro) and torch.equal(l, rl)
+
+
+def test_topk_producer_and_decode_graph_replay(dcp):
+    """A DSA decode step as one graph: every shard's top-k candidates from the indexer
+    scores, their merge into the rows' global top-k, and the fused decode over that top-k.
+    Replays reproduce eager execution bit for bit; the top-k holds k valid, increasing slot
+    ids below each row's visible length."""
+    g = synth.make_decode_problem("g", [5000, 3000], 128, 512, synth.KV_FP8, 4, 1, mtp=2, seed=33,
+                                  device="cuda")
+    D, R, k = g.dcp, g.rows, 512
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    stride = synth.local_len_bound(int(g.row_len.max().item()), D, 1)
+    sc = synth.index_scores(D, R, stride, gen)
+    ll = dcp.dcp_local_lengths(g.row_len, D, 1)
+    cs = torch.empty((D, R, k), dtype=torch.float32, device="cuda")
+    ci = torch.empty((D, R, k), dtype=torch.int32, device="cuda")
+    top = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((R,), dtype=torch.int32, device="cuda")
+    out = torch.empty((R, g.heads, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((R, g.heads), dtype=torch.float32, device="cuda")
+    ws = _ws(dcp, g, top, None, out, lse, D, True)
+
+    def step():
+        dcp.dcp_topk_local(sc, ll, k, D, 1, cand_score=cs, cand_idx=ci)
+        dcp.dcp_topk_merge(cs, ci, k, topk=top, count=cnt)
+        dcp.mla_decode_dcp_fused(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq, g.sm_scale,
+                                 D, 1, idx=top, out=out, lse=lse, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (top, cnt, out, lse)]
+    t_h = top.cpu()
+    assert bool((cnt.cpu() == k).all())
+    assert bool((t_h[:, 1:] > t_h[:, :-1]).all()) and bool((t_h >= 0).all())
+    assert bool((t_h < g.row_len.cpu().unsqueeze(1)).all())
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        for t in (top, cnt, out, lse):
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for t, r in zip((top, cnt, out, lse), ref):
+            assert torch.equal(t, r)
