@@ -82,6 +82,7 @@ struct TcCfg<DCP_KV_BF16> {
 };
 
 constexpr int kTcThreads = 640;
+constexpr int kMinTilesPerPair = 16;
 constexpr int kColO = 0, kColQ = 256, kColS = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kScaleFloor = 8.67361737988403547e-19f;  // 2^-60
@@ -1165,8 +1166,12 @@ int tc_pairs_for(int64_t units, int64_t tiles_bound) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       sms = 148;
   }
+  // at least kMinTilesPerPair tiles per pair: a pair's set-up and pipeline fill cost about as
+  // much as a dozen tiles, and a row cut between pairs adds a split merge (on 16 rows of 16
+  // tiles, 76 pairs of ~3 tiles take 44 us a call, 16 pairs of one row each 31 us)
   int64_t pairs = sms / 2;
-  if (tiles_bound < pairs) pairs = tiles_bound > 0 ? tiles_bound : 1;
+  const int64_t want = (tiles_bound + kMinTilesPerPair - 1) / kMinTilesPerPair;
+  if (want < pairs) pairs = want > 0 ? want : 1;
   (void)units;
   return (int)pairs;
 }
