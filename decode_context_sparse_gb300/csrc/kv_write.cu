@@ -6,10 +6,17 @@
 //
 // One warp per token row.  FP8: lane l holds latent values [16l, 16l+16); the 8 lanes of a
 // 128-value block reduce its amax, scale = amax / 448 (IEEE fp32 division), every value is
-// divided by the scale (IEEE) and rounded to nearest-even E4M3 with saturation at 448 by the
+// divided by the scale and rounded to nearest-even E4M3 with saturation at 448 by the
 // hardware conversion; an all-zero block stores scale 0 and zero codes.  RoPE (64 bf16) is
 // copied.  BF16: the 1152-byte row is copied.  HBM-bound: 1152 B read and 656 / 1152 B
-// written per row.
+// written per row.  A row's data is loaded before its position and block-table entry are
+// resolved, so the three loads overlap.
+//
+// The quotients.  q = v * r with r the correctly rounded 1/scale lies within 2 ulps of the
+// correctly rounded v / scale (two roundings of relative size 2^-24 each).  E4M3 rounding is
+// monotone, so when q - 3 ulps and q + 3 ulps convert to the same code as q, so does the
+// exact quotient; otherwise (q near an E4M3 rounding boundary, about one value in 10^5) that
+// pair is divided exactly.  The codes are those of the IEEE quotients in every case.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,6 +32,23 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// q moved by d units in the last place, away from (d > 0) or towards (d < 0) zero; values
+// within 3 ulps of zero stay put (they are far below the smallest E4M3 step)
+__device__ __forceinline__ float ulp_nudge(float q, int d) {
+  const uint32_t u = __float_as_uint(q);
+  return (u & 0x7fffffffu) < 4u ? q : __uint_as_float(u + d);
+}
+
+// The E4M3 codes of a / s and b / s (IEEE quotients), from products with r = 1 / s.
+__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float a, float b, float s, float r) {
+  const float qa = a * r, qb = b * r;
+  const uint32_t c = f32x2_to_e4m3x2(qa, qb);
+  const uint32_t cl = f32x2_to_e4m3x2(ulp_nudge(qa, -3), ulp_nudge(qb, -3));
+  const uint32_t ch = f32x2_to_e4m3x2(ulp_nudge(qa, 3), ulp_nudge(qb, 3));
+  if (c == cl && c == ch) return c;
+  return f32x2_to_e4m3x2(a / s, b / s);
+}
+
 template <int KVT>
 __global__ void __launch_bounds__(kKvwThreads)
 kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restrict__ seq,
@@ -34,6 +58,18 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kKvwRowsPerCta;
   for (int64_t i = (int64_t)blockIdx.x * kKvwRowsPerCta + (threadIdx.x >> 5); i < n; i += stride) {
+    // the row's data first: its loads overlap the position / block-table chain below
+    const uint4* src = kv + i * (kDqk * 2 / 16);  // 72 chunks of 16 B
+    uint4 d0, d1, d2 = make_uint4(0u, 0u, 0u, 0u);
+    if (KVT == DCP_KV_BF16) {
+      d0 = __ldg(src + lane);
+      d1 = __ldg(src + 32 + lane);
+      if (lane < 8) d2 = __ldg(src + 64 + lane);
+    } else {
+      d0 = __ldg(src + 2 * lane);
+      d1 = __ldg(src + 2 * lane + 1);
+      if (lane < 8) d2 = __ldg(src + 64 + lane);  // RoPE
+    }
     const int t = __ldg(pos + i), b = __ldg(seq + i);
     if (t < 0) continue;  // padding
     if (b < 0 || b >= num_seqs) {
@@ -53,14 +89,14 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
       if (lane == 0) set_err(err, DCP_ERRBIT_PAGE_RANGE);
       continue;
     }
-    const uint4* src = kv + i * (kDqk * 2 / 16);  // 72 chunks of 16 B
     if (KVT == DCP_KV_BF16) {
       uint4* dst = reinterpret_cast<uint4*>(pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesBF16);
-      for (int c = lane; c < 72; c += 32) dst[c] = __ldg(src + c);
+      dst[lane] = d0;
+      dst[32 + lane] = d1;
+      if (lane < 8) dst[64 + lane] = d2;
     } else {
       uint8_t* row = pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesFP8;
-      const uint4 a = __ldg(src + 2 * lane), c = __ldg(src + 2 * lane + 1);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      const uint32_t w[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
       float v[16];
       float amax = 0.f;
 #pragma unroll
@@ -74,15 +110,15 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
       const float scale = amax / 448.0f;
       uint32_t q[4] = {0u, 0u, 0u, 0u};
       if (scale > 0.f) {
+        const float r = 1.0f / scale;  // correctly rounded
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          q[e] = f32x2_to_e4m3x2(v[4 * e] / scale, v[4 * e + 1] / scale) |
-                 (f32x2_to_e4m3x2(v[4 * e + 2] / scale, v[4 * e + 3] / scale) << 16);
+          q[e] = e4m3x2_of_quotients(v[4 * e], v[4 * e + 1], scale, r) |
+                 (e4m3x2_of_quotients(v[4 * e + 2], v[4 * e + 3], scale, r) << 16);
       }
       *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
       if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + 4 * (lane >> 3)) = scale;
-      if (lane < 8)
-        *reinterpret_cast<uint4*>(row + 528 + 16 * lane) = __ldg(src + 64 + lane);
+      if (lane < 8) *reinterpret_cast<uint4*>(row + 528 + 16 * lane) = d2;
     }
   }
 }

@@ -144,3 +144,51 @@ def test_kv_write_then_fused_decode_round_trip(dcp, orc):
                                  1 / 192 ** 0.5, topk=topk, row_len=lens)
     check_out(out, ref_o, "round trip")
     check_lse(lse, ref_l, "round trip")
+
+
+def _reciprocal_traps(limit=8):
+    """(amax, v) with bf16 values for which v * (1/scale) and the IEEE quotient v / scale
+    (scale = amax / 448, fp32) round to different E4M3 codes: a writer that multiplies by the
+    reciprocal without checking gets these wrong.  Found by exhaustive search over bf16 v."""
+    bits = (np.arange(1 << 16, dtype=np.uint32) << 16).view(np.float32)
+    vals = bits[np.isfinite(bits)]
+
+    def e4(x):
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy()
+    out = []
+    for amax in vals[(vals >= 0.5) & (vals <= 300)][::97]:
+        s = np.float32(amax) / np.float32(448)
+        r = np.float32(1) / s
+        v = vals[np.abs(vals) <= amax]
+        bad = e4((v / s).astype(np.float32)) != e4((v * r).astype(np.float32))
+        for x in v[bad][:2]:
+            out.append((float(amax), float(x)))
+        if len(out) >= limit:
+            break
+    return out
+
+
+def test_kv_write_quotients_near_e4m3_boundaries(dcp, orc):
+    """Rows built from values whose reciprocal product rounds to another code than the exact
+    quotient: the written codes must still be those of the IEEE quotients (the oracle's)."""
+    traps = _reciprocal_traps()
+    assert traps, "the search found no trap values"
+    n = len(traps)
+    kv = torch.zeros((n, 576))
+    for i, (amax, v) in enumerate(traps):
+        for b in range(4):
+            kv[i, 128 * b] = amax
+            kv[i, 128 * b + 1:128 * b + 128] = v * (1 if b % 2 == 0 else -1)
+    kv = kv.to(torch.bfloat16)
+    assert all(float(kv[i, 1].abs()) == abs(v) for i, (_, v) in enumerate(traps))
+    seq = torch.zeros(n, dtype=torch.int32)
+    pos = torch.arange(n, dtype=torch.int32)
+    bt = torch.arange(2, dtype=torch.int32).view(1, 1, 2)
+    pool = torch.zeros((2, P, 656), dtype=torch.uint8)
+    ref, written, _ = orc.kv_write(kv, seq, pos, pool, synth.KV_FP8, bt, 1, 1)
+    assert written == n
+    d_pool = pool.cuda()
+    dcp.dcp_kv_cache_write(kv.cuda(), seq.cuda(), pos.cuda(), d_pool, synth.KV_FP8, bt.cuda(), 1, 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_pool.cpu().numpy(), ref)
