@@ -57,7 +57,10 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
                 int32_t* err) {
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kKvwRowsPerCta;
-  for (int64_t i = (int64_t)blockIdx.x * kKvwRowsPerCta + (threadIdx.x >> 5); i < n; i += stride) {
+  const int64_t i0 = (int64_t)blockIdx.x * kKvwRowsPerCta + (threadIdx.x >> 5);
+  // position and sequence of this warp's next row, loaded one row ahead
+  int t_next = i0 < n ? __ldg(pos + i0) : -1, b_next = i0 < n ? __ldg(seq + i0) : -1;
+  for (int64_t i = i0; i < n; i += stride) {
     // the row's data first: its loads overlap the position / block-table chain below
     const uint4* src = kv + i * (kDqk * 2 / 16);  // 72 chunks of 16 B
     uint4 d0, d1, d2 = make_uint4(0u, 0u, 0u, 0u);
@@ -70,7 +73,11 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
       d1 = __ldg(src + 2 * lane + 1);
       if (lane < 8) d2 = __ldg(src + 64 + lane);  // RoPE
     }
-    const int t = __ldg(pos + i), b = __ldg(seq + i);
+    const int t = t_next, b = b_next;
+    if (i + stride < n) {
+      t_next = __ldg(pos + i + stride);
+      b_next = __ldg(seq + i + stride);
+    }
     if (t < 0) continue;  // padding
     if (b < 0 || b >= num_seqs) {
       if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
