@@ -414,24 +414,58 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
     }
     int32_t* out = p.topk + li * p.k;
     if (!__syncthreads_or(unsorted)) {
-      for (int j = tid; j < cnt; j += kTkThreads) {
-        const int x = sorted[j];
-        int lo = 0, hi = p.D - 1;  // the run of entry j
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (sh.run[mid] <= j) lo = mid; else hi = mid - 1;
-        }
-        int pos = j - sh.run[lo];
-        for (int d = 0; d < p.D; ++d) {
-          if (d == lo) continue;
-          int a = sh.run[d], b = sh.run[d + 1];  // smaller ids of run d
-          while (a < b) {
-            const int mid = (a + b) >> 1;
-            if (sorted[mid] < x) a = mid + 1; else b = mid;
+      // merge the runs pairwise, ceil(log2 D) levels between sorted[] and a second buffer,
+      // the last level into the output: each thread takes a slice of the output, finds
+      // where its pair's two runs stand at the slice start (a merge-path binary search) and
+      // merges sequentially from there
+      int32_t* src_b = sorted;
+      int32_t* dst_b = sorted + p.kp;
+      int nr = p.D;
+      const int E = (cnt + kTkThreads - 1) / kTkThreads;
+      if (nr == 1) {
+        for (int j = tid; j < cnt; j += kTkThreads) out[j] = src_b[j];
+      }
+      while (nr > 1) {
+        const bool last = nr <= 2;
+        const int np = (nr + 1) / 2;  // pairs; the last may hold one run
+        const int o0 = tid * E, o1 = min(cnt, o0 + E);
+        if (o0 < o1) {
+          int q = 0, hi = np - 1;  // the pair holding output o0: last q with run[2q] <= o0
+          while (q < hi) {
+            const int mid = (q + hi + 1) >> 1;
+            if (sh.run[2 * mid] <= o0) q = mid; else hi = mid - 1;
           }
-          pos += a - sh.run[d];
+          int ps = sh.run[2 * q], pm = sh.run[min(2 * q + 1, nr)], pe = sh.run[min(2 * q + 2, nr)];
+          const int d = o0 - ps;
+          int lo = max(0, d - (pe - pm)), up = min(d, pm - ps);
+          while (lo < up) {
+            const int mid = (lo + up) >> 1;
+            if (src_b[ps + mid] < src_b[pm + d - mid - 1]) lo = mid + 1; else up = mid;
+          }
+          int ia = ps + lo, ib = pm + d - lo;
+          for (int o = o0; o < o1; ++o) {
+            while (o == pe && q + 1 < np) {  // the slice runs on into the next (non-empty) pair
+              ++q;
+              ps = sh.run[2 * q];
+              pm = sh.run[min(2 * q + 1, nr)];
+              pe = sh.run[min(2 * q + 2, nr)];
+              ia = ps;
+              ib = pm;
+            }
+            const int v = (ib >= pe || (ia < pm && src_b[ia] < src_b[ib])) ? src_b[ia++] : src_b[ib++];
+            if (last) out[o] = v; else dst_b[o] = v;
+          }
         }
-        out[pos] = x;
+        __syncthreads();
+        if (tid == 0) {  // the merged runs' boundaries
+          for (int r = 0; r < np; ++r) sh.run[r] = sh.run[2 * r];
+          sh.run[np] = cnt;
+        }
+        __syncthreads();
+        int32_t* t = src_b;
+        src_b = dst_b;
+        dst_b = t;
+        nr = np;
       }
       for (int j = cnt + tid; j < p.k; j += kTkThreads) out[j] = -1;
     } else {
@@ -463,7 +497,7 @@ size_t tk_smem_bytes(int stage, int kp) { return (size_t)(kTkBins + stage + kp) 
 
 template <bool MERGE>
 cudaError_t tk_launch(const TopkParams& p, int64_t lists, cudaStream_t st) {
-  const size_t smem = tk_smem_bytes(p.stage, MERGE ? p.kp : 0);
+  const size_t smem = tk_smem_bytes(p.stage, MERGE ? 2 * p.kp : 0);  // merge: two run buffers
   // raise the kernel's dynamic shared-memory limit once per device and size
   static int allowed[kTkMaxDevices] = {};
   int dev = 0;
