@@ -4,7 +4,8 @@
 //   mode 1: A in TMEM, B MN-major (B given as [K][N] row-major)  -- the P.V form
 //   mode 2: A in shared memory K-major, B K-major
 //   mode 3: A in shared memory K-major, B MN-major                -- the P.V form, P in smem
-// and a conversion probe for the exact E4M3 -> bf16 (x 2^-112) path.
+// and a conversion probe for the exact E4M3 -> bf16 (x 2^-112) path, and a wait that nothing
+// satisfies, for the bounded mbarrier wait's time limit.
 // Shapes accepted by tc_probe: K in {64, 128} (modes 0, 2) or {16, 32, 64, 128} (modes 1, 3),
 // N a multiple of 16 in [16, 256] (modes 0, 2) or of 64 in [64, 256] (modes 1, 3).
 #include <cuda_runtime.h>
@@ -150,5 +151,36 @@ extern "C" int tc_probe(const void* A, const void* B, float* D, int K, int N, in
 extern "C" int e4m3_probe(const void* codes, void* out, int n) {
   e4m3_probe_kernel<<<(n + 255) / 256, 256>>>(static_cast<const uint16_t*>(codes),
                                                static_cast<uint32_t*>(out), n);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+// Two threads wait on an mbarrier nothing arrives on, with the bounded wait the kernels use:
+// the first gives up after the time limit and sets the abort flag, the second sees the flag
+// and gives up too; the kernel then finishes (no trap, no endless loop).
+// out[0] = waits that returned false, out[1] = the abort flag, out[2] = elapsed ms.
+__global__ void wait_timeout_kernel(int* out) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = globaltimer();
+  __shared__ int gave_up;
+  if (threadIdx.x == 0) gave_up = 0;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0 && !mbar_wait(&bar, 0, &abort_flag)) atomicAdd(&gave_up, 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    out[0] = gave_up;
+    out[1] = abort_flag;
+    out[2] = (int)((globaltimer() - t0) / 1000000ull);
+  }
+}
+
+extern "C" int wait_timeout_probe(int* out) {
+  wait_timeout_kernel<<<1, 64>>>(out);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

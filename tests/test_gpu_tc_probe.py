@@ -1,6 +1,6 @@
 """Probe of the tcgen05 building blocks (TMEM A operand, K-major and MN-major SW128 B
-operands, shared-memory A operand) against torch matmul, and of the exact E4M3 -> bf16
-conversion used by the FP8 tensor-core path."""
+operands, shared-memory A operand) against torch matmul, of the exact E4M3 -> bf16
+conversion used by the FP8 tensor-core path, and of the bounded mbarrier wait running out."""
 import ctypes
 import os
 import subprocess
@@ -25,6 +25,7 @@ def probe():
     lib.tc_probe.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     lib.e4m3_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     lib.e4m3x4_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.wait_timeout_probe.argtypes = [ctypes.c_void_p]
     return lib
 
 
@@ -80,3 +81,16 @@ def test_e4m3x4_to_bf16_exact(probe):
     ref = words.view(torch.uint8).view(65536, 4).view(torch.float8_e4m3fn).double()
     finite = ~torch.isnan(ref)
     assert torch.equal(got[finite], ref[finite])
+
+
+def test_bounded_wait_gives_up_and_reports(probe):
+    """A wait nothing satisfies (an mbarrier no thread arrives on): the bounded wait of the
+    kernels gives up after its 1 s limit and raises the abort flag, a second waiter sees the
+    flag, the kernel finishes, and the context stays usable."""
+    out = torch.zeros(3, dtype=torch.int32, device="cuda")
+    assert probe.wait_timeout_probe(out.data_ptr()) == 0
+    torch.cuda.synchronize()
+    gave_up, flag, ms = out.cpu().tolist()
+    assert gave_up == 2 and flag == 1
+    assert 900 <= ms <= 10000, ms
+    assert (torch.ones(4, device="cuda") * 2).sum().item() == 8.0
