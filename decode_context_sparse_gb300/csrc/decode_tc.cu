@@ -99,7 +99,7 @@ struct TcLay {
   static constexpr int QR_BYTES = 128 * 128;  // RoPE part of Q: 128 rows of one SW128 row
   // exchange rows: TN floats padded to TN + 4 (rows 16-B aligned; a warp's 16-B accesses to
   // one column of 32 rows spread over all banks).  Measured faster than an XOR-swizzled
-  // unpadded layout for the remote st.async stores.
+  // unpadded layout (when the partials still went over as per-thread remote stores).
   static constexpr int XSTRIDE = TN + 4;
   static constexpr int X_BYTES = 128 * XSTRIDE * 4;
   // per K tile: logit scale lo | logit scale hi (fp32, x sl2) | P scales s_lo, s_hi as bf16
@@ -334,7 +334,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // peers' barriers are initialised before any remote arrive / st.async
+  cluster_sync();  // peers' barriers are initialised before any remote arrive or copy
   tc_fence_after();
   const uint32_t tbase = sh.tmem_base;
   const int ntiles = sh.ntiles;
@@ -342,7 +342,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     p.tc_desc[0] = sh.T;
     p.tc_desc[1] = sh.Peff;
   }
-  const int64_t T = sh.T, t0 = sh.t0;
+  const int64_t t0 = sh.t0;
 
   // Loader warps take tiles round-robin; a staging slot's empty barrier is waited on by
   // parity, which tells phases apart only while the barrier is at most one phase behind:

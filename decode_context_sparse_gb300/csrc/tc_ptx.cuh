@@ -330,18 +330,6 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
-// 16-B store into CTA `rank`'s shared memory at the address mirroring `local`, counted
-// (16 bytes) on the barrier mirroring `bar` in that CTA.
-__device__ __forceinline__ void st_async_v4(void* local, uint32_t rank, uint32_t a, uint32_t b,
-                                            uint32_t c, uint32_t d, uint64_t* bar) {
-  asm volatile(
-      "{\n .reg .b32 ra, rb;\n mapa.shared::cluster.u32 ra, %0, %1;\n"
-      " mapa.shared::cluster.u32 rb, %2, %1;\n"
-      " st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [ra], {%3,%4,%5,%6}, [rb];\n}" ::
-          "r"(smem_u32(local)),
-      "r"(rank), "r"(smem_u32(bar)), "r"(a), "r"(b), "r"(c), "r"(d)
-      : "memory");
-}
 
 // Shared memory of this CTA -> the mirrored address in CTA `rank` of the cluster (bytes a
 // multiple of 16, both ends 16-B aligned), completion counted in bytes on the barrier
