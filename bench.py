@@ -134,14 +134,14 @@ def host_copy(prob):
     return prob.to("cpu")
 
 
-def time_oracle_rows(prob_host, budget_s):
-    """Oracle on as many rows of the workload as fit in about budget_s seconds."""
+def time_oracle_rows(prob_host, seconds):
+    """Oracle on as many rows of the workload as fit in about `seconds` of host time."""
     import oracle
     oracle.build()
     t0 = time.perf_counter()
     oracle.attention_problem(prob_host, rows=[0])
     t1 = time.perf_counter() - t0
-    return max(1, min(prob_host.rows, int(budget_s / max(t1, 1e-4))))
+    return max(1, min(prob_host.rows, int(seconds / max(t1, 1e-4))))
 
 
 def run_reference(args):
