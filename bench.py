@@ -211,14 +211,14 @@ def time_kv_cache_write(dcp, dev, peaks, stream, flush, steps):
             "frac": gbs / peaks["hbm_gbs"], "bound": "hbm", "launches_per_call": 1}
 
 
-def time_topk_producer(dcp, dev, peaks, stream, flush, steps):
+def time_topk_producer(dcp, dev, peaks, stream, flush, steps, seqs=64):
     """The DSA top-k producer of the decode batch: every shard's candidate list (8 shards x
     384 rows, 16384 local slots each, k = 2048) and their merge into the rows' global top-k,
     timed like the decode (events, L2 flushed between calls).  Algorithmic bytes: the local
     scores read (4 B per local slot) and the lists written (8 B per candidate); the lists
     read again (8 B) and the top-k written (4 B per entry + 4 B count per row)."""
     import synth
-    p = synth.topk_producer_topk2048(device=dev)
+    p = synth.topk_producer_topk2048(device=dev, seqs=seqs)
     D, k = p.dcp, p.k
     R = p.row_len.numel()
     ll = dcp.dcp_local_lengths(p.row_len, D, p.interleave)
@@ -411,6 +411,9 @@ def main():
     ap.add_argument("--seqs", type=int, default=64,
                     help="sequences of the workload (64 = the full workload; fewer only for "
                          "profiling captures that must stay small)")
+    ap.add_argument("--topk-only", action="store_true",
+                    help="time only the DSA top-k producer (for profiling its kernels) and "
+                         "print its measurement")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -427,6 +430,12 @@ def main():
     dcp.load()
 
     peaks = load_peaks()
+    if args.topk_only:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        res = time_topk_producer(dcp, dev, peaks, torch.cuda.current_stream(dev), flush,
+                                 max(3, args.steps), seqs=args.seqs)
+        print(json.dumps({"topk_producer": res}), flush=True)
+        return
     prob = make_workload(dev, args.seqs)
     kv_bytes, flops, valid = algorithmic(prob)
     R = prob.rows
