@@ -165,6 +165,17 @@ def test_heads_and_dtypes_ragged(dcp, heads, kv):
     _check_problem(dcp, prob)
 
 
+@pytest.mark.parametrize("heads", [48, 80, 96, 112])
+@pytest.mark.parametrize("kv", [synth.KV_BF16, synth.KV_FP8])
+def test_padded_head_counts_tensor_core(dcp, heads, kv):
+    """Head counts the tensor-core path pads to its 128-row tiles (48..112): the padded rows
+    stay out of the outputs, LSEs and split merges.  Rows long enough to be cut between CTA
+    pairs (1000 slots each over a few pairs) exercise the split merge too."""
+    prob = synth.make_decode_problem("padh", [3000, 2200, 130], heads, 1000, kv, 4, 1, mtp=2,
+                                     seed=heads * 3 + kv)
+    _check_problem(dcp, prob)
+
+
 @pytest.mark.parametrize("splits", [1, 3, 64])
 def test_split_counts(dcp, splits):
     prob = synth.make_decode_problem("splits", [3000, 900], 64, 1000, synth.KV_FP8, 4, 1, mtp=3, seed=31)
