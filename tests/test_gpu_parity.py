@@ -176,6 +176,16 @@ def test_padded_head_counts_tensor_core(dcp, heads, kv):
     _check_problem(dcp, prob)
 
 
+@pytest.mark.parametrize("D,I,heads,kv", [(16, 1, 128, synth.KV_FP8), (64, 1, 64, synth.KV_BF16),
+                                           (16, 64, 128, synth.KV_BF16)])
+def test_many_shards(dcp, D, I, heads, kv):
+    """Up to DCP_MAX_SHARDS shards: many shards hold few or no slots of a row (empty
+    partials, -inf LSEs) and the fused path resolves owners across all their tables."""
+    prob = synth.make_decode_problem("manyD", [2500, 700], heads, 300, kv, D, I, mtp=2,
+                                     seed=D * 7 + I + heads)
+    _check_problem(dcp, prob, check_partials=D <= 16)
+
+
 @pytest.mark.parametrize("splits", [1, 3, 64])
 def test_split_counts(dcp, splits):
     prob = synth.make_decode_problem("splits", [3000, 900], 64, 1000, synth.KV_FP8, 4, 1, mtp=3, seed=31)
