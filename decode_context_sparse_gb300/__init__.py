@@ -36,7 +36,8 @@ TOKEN_BYTES = {DCP_KV_BF16: 1152, DCP_KV_FP8_E4M3_S128: 656}
 EXPORTS = ("dcp_status_string", "dcp_abi_version", "dcp_remap_topk", "dcp_local_lengths",
            "mla_decode_partial_lse", "dcp_lse_merge", "mla_decode_dcp_fused",
            "mla_decode_workspace_size", "mla_decode_dcp_fused_noalloc", "dcp_kv_cache_write",
-           "dcp_topk_local", "dcp_topk_merge")
+           "dcp_topk_local", "dcp_topk_merge", "mla_prefill_chunk_workspace_size",
+           "mla_prefill_chunk_dcp")
 DCP_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -100,6 +101,10 @@ def load(path: str = LIB_PATH):
     lib.dcp_topk_local.argtypes = [V, I64, I32, V, I32, I32, I32, I32, V, V, V]
     lib.dcp_topk_merge.restype = ctypes.c_int
     lib.dcp_topk_merge.argtypes = [V, V, I32, I64, I32, I32, V, V, V]
+    lib.mla_prefill_chunk_workspace_size.restype = SZ
+    lib.mla_prefill_chunk_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32]
+    lib.mla_prefill_chunk_dcp.restype = ctypes.c_int
+    lib.mla_prefill_chunk_dcp.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32, V]
     lib.mla_decode_workspace_size.restype = SZ
     lib.mla_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs), I32, I32]
     if lib.dcp_abi_version() != DCP_ABI_VERSION:
@@ -380,32 +385,30 @@ def mla_decode_dcp_fused(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, d
 
 
 def mla_prefill_chunk_dcp(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, dcp, interleave, *,
-                          prefix_len, chunk_idx, max_prefix_len, out=None, lse=None, stream=None):
-    """Attention of a prefill chunk's query rows under DCP, as partials merged by LSE.
-
-    Row r attends to its sequence's cached prefix, global slots [0, prefix_len[r]) held by the
-    D shards under the owner rule (one dense partial per shard, over that shard's local
-    slots), and to the slots of the chunk it sees, chunk_idx[r] (global ids, -1 padded; one
-    sparse partial per shard after the remap).  The 2*dcp partials are merged with LSE
-    weights.  Steps: dcp_local_lengths, mla_decode_partial_lse (dense), dcp_remap_topk,
-    mla_decode_partial_lse (sparse), dcp_lse_merge.  max_prefix_len bounds prefix_len on
-    the host (no device read).  Returns (out [R, H, 512] bf16, lse [R, H] fp32)."""
+                          prefix_len, chunk_idx, max_prefix_len, out=None, lse=None, workspace=None,
+                          stream=None):
+    """Attention of a prefill chunk's query rows under DCP (the C entry of the same name):
+    row r over its sequence's cached prefix [0, prefix_len[r]) and over the chunk slots
+    chunk_idx[r] (global ids, -1 padded), per-shard partials merged by LSE.
+    max_prefix_len bounds prefix_len on the host.  Returns (out [R, H, 512] bf16, lse [R, H])."""
     R, H, _ = q.shape
-    _i32(prefix_len, "prefix_len")
-    _i32(chunk_idx, "chunk_idx")
-    po = torch.empty((2 * dcp, R, H, 512), dtype=torch.float32, device=q.device)
-    pl = torch.empty((2 * dcp, R, H), dtype=torch.float32, device=q.device)
-    # the longest local prefix any shard holds (slot counts of one owner are at most
-    # interleave * ceil(L / (interleave * dcp)))
-    local_max = interleave * -(-int(max_prefix_len) // (interleave * dcp))
-    ll = dcp_local_lengths(prefix_len, dcp, interleave, stream=stream)
-    mla_decode_partial_lse(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, kv_len=ll,
-                           max_kv_len=local_max, num_shards=dcp, out=po[:dcp], lse=pl[:dcp],
-                           stream=stream)
-    loc, cnt = dcp_remap_topk(chunk_idx, dcp, interleave, stream=stream)
-    mla_decode_partial_lse(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx=loc,
-                           count=cnt, num_shards=dcp, out=po[dcp:], lse=pl[dcp:], stream=stream)
-    return dcp_lse_merge(po, pl, out=out, lse=lse, stream=stream)
+    if out is None:
+        out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
+    a = _decode_args(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, chunk_idx, None, None,
+                     None, out, lse, 0, False, None)
+    a.kv_len = _ptr(_i32(prefix_len, "prefix_len")).value
+    a.max_kv_len = int(max_prefix_len)
+    need = load().mla_prefill_chunk_workspace_size(ctypes.byref(a), dcp, interleave)
+    if need == ctypes.c_size_t(-1).value:
+        raise DcpError(DCP_ERR_INVALID_ARG, "mla_prefill_chunk_workspace_size")
+    ws = workspace if workspace is not None else _workspace(need, q.device)
+    a.workspace = _ptr(ws).value
+    a.workspace_bytes = ws.numel() * ws.element_size()
+    _check(load().mla_prefill_chunk_dcp(ctypes.byref(a), dcp, interleave, _stream(stream)),
+           "mla_prefill_chunk_dcp")
+    return out, lse
 
 
 def mla_decode_dcp_fused_noalloc(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, dcp,

@@ -229,6 +229,122 @@ int dcp_lse_merge(const float* part_out, const float* part_lse, int32_t dcp, int
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Workspace of mla_prefill_chunk_dcp: local prefix lengths, remapped chunk slots and their
+// counts, the 2*dcp partial outputs and LSEs, and the partial decode calls' own workspace.
+struct PrefillWs {
+  size_t ll, loc, cnt, po, pl, dws, total;
+};
+
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// The two partial decode calls of a prefill chunk (the caller fills pointers later).
+void prefill_calls(const dcp_mla_decode_args* a, int32_t dcp, int32_t interleave,
+                   dcp_mla_decode_args& dense, dcp_mla_decode_args& sparse) {
+  dense = *a;
+  dense.idx = nullptr;
+  dense.count = nullptr;
+  // a shard holds at most interleave * ceil(L / (interleave * dcp)) of L slots
+  const int64_t id = (int64_t)interleave * dcp;
+  dense.max_kv_len = (int32_t)(interleave * ((a->max_kv_len + id - 1) / id));
+  dense.num_splits = a->num_splits;
+  sparse = *a;
+  sparse.kv_len = nullptr;
+  sparse.max_kv_len = 0;
+}
+
+bool prefill_layout(const dcp_mla_decode_args* a, int32_t dcp, int32_t interleave, PrefillWs& w) {
+  const size_t R = (size_t)a->rows, H = (size_t)a->heads, D = (size_t)dcp, K = (size_t)a->k;
+  w.ll = 0;
+  w.loc = w.ll + a256(D * R * 4);
+  w.cnt = w.loc + a256(D * R * K * 4);
+  w.po = w.cnt + a256(D * R * 4);
+  w.pl = w.po + a256(2 * D * R * H * kDv * 4);
+  w.dws = w.pl + a256(2 * D * R * H * 4);
+  dcp_mla_decode_args dense, sparse;
+  prefill_calls(a, dcp, interleave, dense, sparse);
+  // the partial calls' workspace sizes depend on shapes only: stand-in pointers suffice
+  int32_t* fake = reinterpret_cast<int32_t*>((uintptr_t)256);
+  dense.kv_len = fake;
+  sparse.idx = fake;
+  sparse.count = fake;
+  const size_t n1 = mla_decode_workspace_size(&dense, dcp, 0);
+  const size_t n2 = mla_decode_workspace_size(&sparse, dcp, 0);
+  if (n1 == (size_t)-1 || n2 == (size_t)-1) return false;
+  w.total = w.dws + a256(n1 > n2 ? n1 : n2);
+  return true;
+}
+
+int prefill_check(const dcp_mla_decode_args* a, int32_t dcp, int32_t interleave) {
+  if (a == nullptr) return DCP_ERR_INVALID_ARG;
+  if (!valid_rule(dcp, interleave)) return DCP_ERR_INVALID_ARG;
+  if (2 * dcp > DCP_MAX_SHARDS) return DCP_ERR_UNSUPPORTED;  // the merge takes 2*dcp partials
+  if (a->idx == nullptr || a->kv_len == nullptr || a->max_kv_len < 0) return DCP_ERR_INVALID_ARG;
+  if (a->k < 1 || a->k > DCP_MAX_TOPK || a->rows < 0) return DCP_ERR_INVALID_ARG;
+  return DCP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_prefill_chunk_workspace_size(const dcp_mla_decode_args* args, int32_t dcp,
+                                        int32_t interleave) {
+  if (prefill_check(args, dcp, interleave) != DCP_OK) return (size_t)-1;
+  PrefillWs w;
+  if (!prefill_layout(args, dcp, interleave, w)) return (size_t)-1;
+  return w.total;
+}
+
+int mla_prefill_chunk_dcp(const dcp_mla_decode_args* args, int32_t dcp, int32_t interleave,
+                          dcp_stream_t stream) {
+  int rc = prefill_check(args, dcp, interleave);
+  if (rc != DCP_OK) return rc;
+  PrefillWs w;
+  if (!prefill_layout(args, dcp, interleave, w)) return DCP_ERR_INVALID_ARG;
+  if (args->workspace == nullptr || args->workspace_bytes < w.total || !aligned(args->workspace, 256))
+    return DCP_ERR_WORKSPACE;
+  if (!args->out || !args->lse || !aligned(args->out, 8) || !aligned(args->lse, 4))
+    return DCP_ERR_INVALID_ARG;
+  if (args->rows == 0) return DCP_OK;
+  uint8_t* ws = static_cast<uint8_t*>(args->workspace);
+  int32_t* ll = reinterpret_cast<int32_t*>(ws + w.ll);
+  int32_t* loc = reinterpret_cast<int32_t*>(ws + w.loc);
+  int32_t* cnt = reinterpret_cast<int32_t*>(ws + w.cnt);
+  float* po = reinterpret_cast<float*>(ws + w.po);
+  float* pl = reinterpret_cast<float*>(ws + w.pl);
+  const size_t dws_bytes = w.total - w.dws;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t R = args->rows, H = args->heads;
+  dcp_mla_decode_args dense, sparse;
+  prefill_calls(args, dcp, interleave, dense, sparse);
+  // 1-2. the cached prefix: each shard's local length, one dense partial per shard
+  if ((rc = status_of(launch_local_lengths(args->kv_len, R, dcp, interleave, -1, ll, st))) != DCP_OK)
+    return rc;
+  dense.kv_len = ll;
+  dense.out = po;
+  dense.lse = pl;
+  dense.workspace = ws + w.dws;
+  dense.workspace_bytes = dws_bytes;
+  if ((rc = mla_decode_partial_lse(&dense, dcp, stream)) != DCP_OK) return rc;
+  // 3-4. the chunk: each shard's slots of it, one sparse partial per shard
+  if ((rc = status_of(launch_remap_topk(args->idx, R, args->k, dcp, interleave, -1, loc, cnt, st))) !=
+      DCP_OK)
+    return rc;
+  sparse.idx = loc;
+  sparse.count = cnt;
+  sparse.out = po + (int64_t)dcp * R * H * kDv;
+  sparse.lse = pl + (int64_t)dcp * R * H;
+  sparse.workspace = ws + w.dws;
+  sparse.workspace_bytes = dws_bytes;
+  if ((rc = mla_decode_partial_lse(&sparse, dcp, stream)) != DCP_OK) return rc;
+  // 5. the LSE merge of the 2*dcp partials
+  return status_of(launch_lse_merge(po, pl, 2 * dcp, R, (int)H, kDv, args->out, args->lse, st));
+}
+
 size_t mla_decode_workspace_size(const dcp_mla_decode_args* args, int32_t num_shards_or_dcp,
                                  int32_t fused) {
   DecodeParams p;

@@ -318,6 +318,29 @@ int mla_decode_dcp_fused_noalloc(const dcp_mla_decode_args* args, int32_t dcp,
                                  int32_t interleave, dcp_stream_t stream);
 
 /*
+ * mla_prefill_chunk_dcp -- attention of a prefill chunk's query rows under DCP, as partials
+ * merged with LSE weights.
+ * Passage: LMDeploy PR #4952, Summary (prefill gathers the cached-prefix KV in bounded
+ *   chunks; partial attention results merge with LSE weights).
+ *
+ * Row r attends to its sequence's cached prefix, global slots [0, kv_len[r]), and to the
+ * chunk slots idx[r][0..k) it sees (global ids, -1 padded; the chunk tokens' KV already in
+ * the pool).  Steps, on `stream`: each shard's local prefix length; one dense partial per
+ * shard over its prefix slots; each shard's chunk slots (the remap); one sparse partial per
+ * shard over them; the LSE merge of the 2*dcp partials into out / lse.
+ * args: as mla_decode_dcp_fused, with kv_len = the rows' prefix lengths (device, [rows]
+ *   int32), max_kv_len >= every one of them, idx / k = the chunk slots, block_table
+ *   [dcp][num_seqs][bt_stride]; out [rows][heads][512] bf16, lse [rows][heads] fp32;
+ *   workspace of mla_prefill_chunk_workspace_size bytes, 256-B aligned.
+ * Errors: as mla_decode_dcp_fused; DCP_ERR_INVALID_ARG without idx or kv_len;
+ *   DCP_ERR_UNSUPPORTED for dcp > DCP_MAX_SHARDS / 2 (the merge takes 2*dcp partials).
+ */
+size_t mla_prefill_chunk_workspace_size(const dcp_mla_decode_args* args, int32_t dcp,
+                                        int32_t interleave);
+int mla_prefill_chunk_dcp(const dcp_mla_decode_args* args, int32_t dcp, int32_t interleave,
+                          dcp_stream_t stream);
+
+/*
  * mla_decode_workspace_size -- bytes of workspace a decode call with these arguments
  * needs (0 when none).  fused = 0 for mla_decode_partial_lse (num_shards_or_dcp =
  * num_shards), 1 for mla_decode_dcp_fused (num_shards_or_dcp = dcp).  Returns

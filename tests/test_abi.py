@@ -168,3 +168,19 @@ def test_topk_entries_reject_bad_arguments(lib):
     assert run_m(dcp=64, kin=1 << 26) == E          # D * k_in past INT32_MAX
     assert run_m(top=bad) == E
     assert run_m(rows=0) == dcp.DCP_OK
+
+
+def test_prefill_chunk_entry_checks(lib):
+    import decode_context_sparse_gb300 as dcp
+    R = ctypes.byref
+    E = dcp.DCP_ERR_INVALID_ARG
+    good = dict(kv_len=1 << 20, max_kv_len=5000)
+    assert lib.mla_prefill_chunk_workspace_size(R(_args(**good)), 8, 1) > 0
+    assert lib.mla_prefill_chunk_workspace_size(R(_args(idx=None, **good)), 8, 1) == \
+        ctypes.c_size_t(-1).value
+    assert lib.mla_prefill_chunk_dcp(None, 8, 1, None) == E
+    assert lib.mla_prefill_chunk_dcp(R(_args(**good)), 8, 1, None) == dcp.DCP_ERR_WORKSPACE
+    assert lib.mla_prefill_chunk_dcp(R(_args(**good)), 33, 1, None) == dcp.DCP_ERR_UNSUPPORTED
+    assert lib.mla_prefill_chunk_dcp(R(_args(max_kv_len=5000)), 8, 1, None) == E   # no prefix lengths
+    assert lib.mla_prefill_chunk_dcp(R(_args(idx=None, **good)), 8, 1, None) == E   # no chunk slots
+    assert lib.mla_prefill_chunk_dcp(R(_args(**good)), 8, 0, None) == E            # interleave 0
