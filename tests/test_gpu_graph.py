@@ -4,11 +4,15 @@ and allocation-free (the workspace is sized and allocated before capture), so a 
 records into one graph.  The remap of a row's top-k is
 computed once per step and reused by every layer (the indices are the same for all layers
 of a step).  Replays must reproduce eager execution bit for bit (the kernels are
-deterministic for a fixed launch shape)."""
+deterministic for a fixed launch shape), and the replayed results must match the oracle
+within the parity tolerances (top-k bit-exact)."""
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
+from parity import check_lse, check_out
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +63,9 @@ def test_fused_decode_graph_replay_matches_eager(dcp, kind):
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    ro, rl = oracle.attention_problem(g)
+    check_out(out, ro, "graph replay out")
+    check_lse(lse, rl, "graph replay lse")
 
 
 def test_multi_layer_step_graph_with_shared_remap(dcp):
@@ -104,6 +111,12 @@ def test_multi_layer_step_graph_with_shared_remap(dcp):
     torch.cuda.synchronize()
     for (ro, rl), o, l in zip(ref, outs, lses):
         assert torch.equal(o, ro) and torch.equal(l, rl)
+    for i, (p, o, l) in enumerate(zip(probs, outs, lses)):
+        # layer i attends over its own cache with the step's shared top-k
+        p.topk = topk
+        wo, wl = oracle.attention_problem(p)
+        check_out(o, wo, "graph replay layer %d out" % i)
+        check_lse(l, wl, "graph replay layer %d lse" % i)
 
 
 def test_topk_producer_and_decode_graph_replay(dcp):
@@ -153,3 +166,11 @@ def test_topk_producer_and_decode_graph_replay(dcp):
         torch.cuda.synchronize()
         for t, r in zip((top, cnt, out, lse), ref):
             assert torch.equal(t, r)
+    from oracle import topk as otk
+    ws_, wi_ = otk.local_topk(sc.cpu().numpy(), ll.cpu().numpy(), k, D, 1)
+    wt, wc = otk.merge_topk(ws_, wi_, k)
+    assert np.array_equal(top.cpu().numpy(), wt) and np.array_equal(cnt.cpu().numpy(), wc)
+    g.topk = torch.from_numpy(wt).cuda()
+    ro, rl = oracle.attention_problem(g)
+    check_out(out, ro, "graph replay dsa step out")
+    check_lse(lse, rl, "graph replay dsa step lse")

@@ -1,5 +1,5 @@
 """GPU parity: the CUDA path through the C ABI against the oracle, element by element on
-small and ragged cases, and on sampled rows at the full workload sizes."""
+small and ragged cases and on every row of the full-size workloads."""
 import math
 
 import numpy as np
@@ -66,18 +66,15 @@ def test_local_lengths(dcp):
 # ----------------------------------------------------------------------------- merge
 @pytest.mark.parametrize("D", [2, 4, 8])
 def test_merge_stress_full_size(dcp, D):
+    """Every row of the remap + merge stress workload (256 rows x 128 heads x 512)."""
     prob = synth.cfg4_remap_merge(D, device=DEV)
     out, lse = dcp.dcp_lse_merge(prob.part_out, prob.part_lse)
     torch.cuda.synchronize()
     R = prob.part_out.shape[1]
-    lse_np = prob.part_lse.cpu().numpy()
-    empty_some = np.where(np.isneginf(lse_np[:, :, 0]).any(axis=0))[0]
-    rows = sorted(set([0, R // 2, R - 1] + list(empty_some[:12]) + list(range(1, R, 37))))
-    ro, rl = oracle.merge(prob.part_out[:, rows].cpu().numpy(), lse_np[:, rows])
-    check_out(out[rows], ro, "merge out")
-    check_lse(lse[rows], rl, "merge lse")
+    ro, rl = oracle.merge(prob.part_out.cpu().numpy(), prob.part_lse.cpu().numpy())
+    check_out(out, ro, "merge out")
+    check_lse(lse, rl, "merge lse")
     assert torch.all(out[R // 2] == 0) and torch.all(torch.isneginf(lse[R // 2]))
-    assert not torch.isnan(out.float()).any()
 
 
 @pytest.mark.parametrize("dv", [512, 4, 132])
@@ -238,30 +235,29 @@ def test_checked_mode_reports_bad_pages(dcp):
 
 
 # ----------------------------------------------------------------------------- full size
-def _sampled_full(dcp, prob, rows):
+def _full_size(dcp, prob):
+    """Every row of a full-size workload: fused and merged outputs against unsharded
+    attention, and every shard's partials against the oracle restricted to that shard."""
     g = prob.to(DEV) if not prob.q.is_cuda else prob
     fo, fl = run_fused(dcp, g)
     po, pl, mo, ml = run_unfused(dcp, g)
     torch.cuda.synchronize()
-    host = synth.DecodeProblem(prob.name, prob.rows, prob.heads, prob.dcp, prob.interleave,
-                               prob.page_size, prob.kv_dtype, prob.sm_scale, g.q.cpu(),
-                               g.pool.cpu(), g.block_table.cpu(), g.row_seq.cpu(), g.row_len.cpu(),
-                               None if g.topk is None else g.topk.cpu(), g.seq_len.cpu())
-    ro, rl = oracle.attention_problem(host, rows=rows)
-    check_out(fo[rows], ro, "fused out")
-    check_lse(fl[rows], rl, "fused lse")
-    check_out(mo[rows], ro, "merged out")
-    check_lse(ml[rows], rl, "merged lse")
-    so, sl = oracle.attention_problem(host, rows=rows[:2], shard=prob.dcp - 1)
-    check_out(po[prob.dcp - 1][rows[:2]], so, "partial out")
-    check_lse(pl[prob.dcp - 1][rows[:2]], sl, "partial lse")
+    host = g.to("cpu")
+    ro, rl = oracle.attention_problem(host)
+    check_out(fo, ro, "fused out")
+    check_lse(fl, rl, "fused lse")
+    check_out(mo, ro, "merged out")
+    check_lse(ml, rl, "merged lse")
+    del ro, rl, fo, fl, mo, ml
+    for s in range(prob.dcp):
+        so, sl = oracle.attention_problem(host, shard=s)
+        check_out(po[s], so, "partial out shard %d" % s)
+        check_lse(pl[s], sl, "partial lse shard %d" % s)
 
 
-def test_cfg3_full_size_sampled_rows(dcp):
-    prob = synth.cfg3_sparse_topk2048_fp8(device=DEV)
-    _sampled_full(dcp, prob, [0, 5, 77, 200, 383])
+def test_cfg3_full_size_all_rows(dcp):
+    _full_size(dcp, synth.cfg3_sparse_topk2048_fp8(device=DEV))
 
 
-def test_cfg5_full_size_sampled_rows(dcp):
-    prob = synth.cfg5_dense_long(device=DEV)
-    _sampled_full(dcp, prob, [0, 13, 31])
+def test_cfg5_full_size_all_rows(dcp):
+    _full_size(dcp, synth.cfg5_dense_long(device=DEV))
