@@ -44,8 +44,8 @@ def load_peaks():
 
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons sampled every ~2 ms through NVML (read-only
-    queries via ctypes) in a background thread while the timed region runs; falls back to
-    nvidia-smi polling when NVML cannot be loaded."""
+    queries via ctypes) in a background thread while the timed region runs.  Without NVML it
+    records no samples and says so in its result."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
@@ -116,7 +116,11 @@ def dist_env():
     return ws, rank, local
 
 
-TRAFFIC_BYTES_PER_ROW = (167.572736e6 + 16.186112e6) / 96
+# DRAM traffic of the decode kernel (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of a 96-row slice of this workload (bench.py --seqs 16), per decode row; the bench
+# scales it to the full launch by rows, since the traffic grows with the rows processed.
+TRAFFIC_CAPTURE = {"bytes_per_row": (167.572736e6 + 16.186112e6) / 96, "rows": 96,
+                   "kernel": "decode_tc_kernel<FP8, fused, sparse>"}
 
 
 def make_workload(dev, seqs=64):
@@ -411,6 +415,9 @@ def main():
     ap.add_argument("--seqs", type=int, default=64,
                     help="sequences of the workload (64 = the full workload; fewer only for "
                          "profiling captures that must stay small)")
+    ap.add_argument("--kernel-path", default="auto", choices=["auto", "cuda_cores"],
+                    help="decode kernel choice passed to every decode call (cuda_cores: the "
+                         "CUDA-core kernel for every head count, for profiling it)")
     ap.add_argument("--topk-only", action="store_true",
                     help="time only the DSA top-k producer (for profiling its kernels) and "
                          "print its measurement")
@@ -445,10 +452,12 @@ def main():
     out = torch.empty((R, prob.heads, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((R, prob.heads), dtype=torch.float32, device=dev)
 
+    kpath = dcp.DCP_PATH_CUDA_CORES if args.kernel_path == "cuda_cores" else dcp.DCP_PATH_AUTO
+
     def step():
         dcp.mla_decode_dcp_fused(prob.q, prob.pool, prob.kv_dtype, prob.block_table, prob.row_seq,
                                  prob.sm_scale, prob.dcp, prob.interleave, idx=prob.topk,
-                                 out=out, lse=lse)
+                                 out=out, lse=lse, kernel_path=kpath)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -486,7 +495,7 @@ def main():
         dcp.dcp_remap_topk(prob.topk, D, prob.interleave, local_idx=loc, count=cnt)
         dcp.mla_decode_partial_lse(prob.q, prob.pool, prob.kv_dtype, prob.block_table,
                                    prob.row_seq, prob.sm_scale, idx=loc, count=cnt, num_shards=D,
-                                   out=po, lse=pl)
+                                   out=po, lse=pl, kernel_path=kpath)
         dcp.dcp_lse_merge(po, pl, out=out, lse=lse)
 
     for _ in range(3):
@@ -610,10 +619,20 @@ def main():
     else:
         roof = {"bound": "hbm", "achieved": hbm_tbs * 1e3, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": hbm_tbs * 1e3 / peaks["hbm_gbs"]}
-    # DRAM bytes (read + write) per launch from ncu (profiles/decode_tc_fused_topk2048_fp8_96rows.md:
-    # 167.6 MB + 16.2 MB for 96 rows), scaled by rows: traffic grows with the rows processed.
-    roof["traffic"] = TRAFFIC_BYTES_PER_ROW * R if prob.heads == 128 else None
+    # traffic: the ncu capture's DRAM bytes per row times the rows of this launch (not
+    # measured in this run; see TRAFFIC_CAPTURE), beside the algorithmic bytes it compares to
+    alg_all = kv_bytes + prob.q.numel() * 2 + out.numel() * 2 + lse.numel() * 4 + \
+        prob.topk.numel() * 4
+    traffic = TRAFFIC_CAPTURE["bytes_per_row"] * R if prob.heads == 128 else None
+    roof["traffic"] = traffic
     roof["traffic_unit"] = "bytes"
+    roof["traffic_src"] = ("ncu capture of %s on a %d-row slice of this workload, scaled to %d "
+                           "rows" % (TRAFFIC_CAPTURE["kernel"], TRAFFIC_CAPTURE["rows"], R))
+    roof["algorithmic_bytes_kv"] = kv_bytes
+    roof["algorithmic_bytes_all"] = alg_all
+    if traffic is not None:
+        roof["traffic_over_kv"] = traffic / kv_bytes
+        roof["traffic_over_all"] = traffic / alg_all
     roof["peak_src"] = peaks["src"]
     roof["kernel"] = "mla_decode_dcp_fused"
     roof["roofline_us"] = 1e6 * max(t_hbm, t_tc)

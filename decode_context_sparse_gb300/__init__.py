@@ -29,7 +29,9 @@ DCP_ERRBIT_PAGE_RANGE = 2
 DCP_ERRBIT_TIMEOUT = 4
 DCP_MAX_SHARDS = 64
 DCP_MAX_TOPK = 16384
-DCP_ABI_VERSION = 1
+DCP_ABI_VERSION = 2
+DCP_PATH_AUTO = 0          # tensor cores for 48..128 heads, CUDA cores otherwise
+DCP_PATH_CUDA_CORES = 1    # the CUDA-core kernel for every head count
 TOKEN_BYTES = {DCP_KV_BF16: 1152, DCP_KV_FP8_E4M3_S128: 656}
 
 # every symbol include/dcpmla.h declares
@@ -62,6 +64,7 @@ class DecodeArgs(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("num_splits", ctypes.c_int32),
         ("checked", ctypes.c_int32), ("err_flag", ctypes.c_void_p),
+        ("kernel_path", ctypes.c_int32),
     ]
 
 
@@ -135,9 +138,11 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream, device=None) -> ctypes.c_void_p:
+    """The stream handle a call runs on: `stream` (a torch.cuda.Stream or a raw handle), else
+    the current stream of `device` (the device of the call's tensors)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
@@ -160,7 +165,8 @@ def dcp_remap_topk(global_idx: torch.Tensor, dcp: int, interleave: int, shard: i
     if count is None:
         count = torch.empty((n_out, rows), dtype=torch.int32, device=global_idx.device)
     _check(load().dcp_remap_topk(_ptr(global_idx), rows, k, dcp, interleave, shard,
-                                 _ptr(local_idx), _ptr(count), _stream(stream)), "dcp_remap_topk")
+                                 _ptr(local_idx), _ptr(count), _stream(stream, global_idx.device)),
+           "dcp_remap_topk")
     return local_idx, count
 
 
@@ -173,7 +179,8 @@ def dcp_local_lengths(global_len: torch.Tensor, dcp: int, interleave: int, shard
     if local_len is None:
         local_len = torch.empty((n_out, rows), dtype=torch.int32, device=global_len.device)
     _check(load().dcp_local_lengths(_ptr(global_len), rows, dcp, interleave, shard,
-                                    _ptr(local_len), _stream(stream)), "dcp_local_lengths")
+                                    _ptr(local_len), _stream(stream, global_len.device)),
+           "dcp_local_lengths")
     return local_len
 
 
@@ -195,7 +202,8 @@ def dcp_topk_local(scores: torch.Tensor, local_len: torch.Tensor, k: int, dcp: i
     if cand_idx is None:
         cand_idx = torch.empty((n_in, rows, k), dtype=torch.int32, device=scores.device)
     _check(load().dcp_topk_local(_ptr(scores), rows, stride, _ptr(local_len), k, dcp, interleave,
-                                 shard, _ptr(cand_score), _ptr(cand_idx), _stream(stream)),
+                                 shard, _ptr(cand_score), _ptr(cand_idx),
+                                 _stream(stream, scores.device)),
            "dcp_topk_local")
     return cand_score, cand_idx
 
@@ -217,7 +225,8 @@ def dcp_topk_merge(cand_score: torch.Tensor, cand_idx: torch.Tensor, k: Optional
     if count is None:
         count = torch.empty((rows,), dtype=torch.int32, device=cand_score.device)
     _check(load().dcp_topk_merge(_ptr(cand_score), _ptr(cand_idx), D, rows, k_in, k, _ptr(topk),
-                                 _ptr(count), _stream(stream)), "dcp_topk_merge")
+                                 _ptr(count), _stream(stream, cand_score.device)),
+           "dcp_topk_merge")
     return topk, count
 
 
@@ -255,7 +264,8 @@ def dcp_kv_cache_write(kv: torch.Tensor, seq: torch.Tensor, pos: torch.Tensor, k
     _check(load().dcp_kv_cache_write(_ptr(kv), n, _ptr(seq), _ptr(pos), dcp, interleave, shard,
                                      _ptr(kv_pool), num_pages, kv_dtype, page_size, _ptr(block_table),
                                      block_table.shape[1], block_table.shape[2], 1 if checked else 0,
-                                     _ptr(err_flag), _stream(stream)), "dcp_kv_cache_write")
+                                     _ptr(err_flag), _stream(stream, kv.device)),
+           "dcp_kv_cache_write")
     return kv_pool
 
 
@@ -271,7 +281,7 @@ def dcp_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out: Optional[
     if lse is None:
         lse = torch.empty((R, H), dtype=torch.float32, device=part_out.device)
     _check(load().dcp_lse_merge(_ptr(part_out), _ptr(part_lse), D, R, H, dv, _ptr(out), _ptr(lse),
-                                _stream(stream)), "dcp_lse_merge")
+                                _stream(stream, part_out.device)), "dcp_lse_merge")
     return out, lse
 
 
@@ -279,11 +289,12 @@ def dcp_lse_merge(part_out: torch.Tensor, part_lse: torch.Tensor, out: Optional[
 _ws_cache = {}
 
 
-def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
-    """A zero-initialised workspace reused across calls (the kernels leave it ready)."""
+def _workspace(nbytes: int, device, stream: ctypes.c_void_p) -> Optional[torch.Tensor]:
+    """A workspace reused by the calls on one (device, stream): calls on one stream run one
+    after another, so they may share it; calls on different streams get their own."""
     if nbytes == 0:
         return None
-    key = (str(device), torch.cuda.current_stream(device).cuda_stream)
+    key = (str(device), stream.value)
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
@@ -292,7 +303,7 @@ def _workspace(nbytes: int, device) -> Optional[torch.Tensor]:
 
 
 def _decode_args(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx, count, kv_len,
-                 max_kv_len, out, lse, num_splits, checked, err_flag):
+                 max_kv_len, out, lse, num_splits, checked, err_flag, kernel_path=DCP_PATH_AUTO):
     if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != 576:
         raise ValueError("q must be [rows, heads, 576] bf16")
     if kv_pool.dtype != torch.uint8 or kv_pool.dim() != 3:
@@ -320,14 +331,18 @@ def _decode_args(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx, coun
         a.k = idx.shape[-1]
         if count is not None:
             a.count = _ptr(_i32(count, "count")).value
-    else:
+    elif kv_len is not None:
+        if max_kv_len is None:
+            raise ValueError("dense calls must pass max_kv_len, an upper bound of kv_len "
+                             "(reading it from the device tensor would synchronise)")
         a.kv_len = _ptr(_i32(kv_len, "kv_len")).value
-        a.max_kv_len = int(max_kv_len) if max_kv_len is not None else int(kv_len.max().item())
+        a.max_kv_len = int(max_kv_len)
     a.out = _ptr(out).value
     a.lse = _ptr(lse).value
     a.num_splits = int(num_splits)
     a.checked = 1 if checked else 0
     a.err_flag = _ptr(err_flag).value if err_flag is not None else None
+    a.kernel_path = int(kernel_path)
     return a
 
 
@@ -338,10 +353,10 @@ def mla_decode_workspace_size(args: DecodeArgs, num_shards_or_dcp: int, fused: b
     return int(n)
 
 
-def _bind_ws(a: DecodeArgs, n: int, fused: bool, device, workspace):
+def _bind_ws(a: DecodeArgs, n: int, fused: bool, device, workspace, stream):
     need = mla_decode_workspace_size(a, n, fused)
     if need:
-        ws = workspace if workspace is not None else _workspace(need, device)
+        ws = workspace if workspace is not None else _workspace(need, device, stream)
         a.workspace = _ptr(ws).value
         a.workspace_bytes = ws.numel() * ws.element_size()
     return need
@@ -350,37 +365,40 @@ def _bind_ws(a: DecodeArgs, n: int, fused: bool, device, workspace):
 def mla_decode_partial_lse(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, *, idx=None,
                            count=None, kv_len=None, max_kv_len=None, num_shards=1, out=None,
                            lse=None, workspace=None, num_splits=0, checked=False, err_flag=None,
-                           stream=None):
+                           kernel_path=DCP_PATH_AUTO, stream=None):
     """Per-shard MLA decode with LSE.  block_table [S,B,maxp]; sparse: idx [S,R,K] local ids +
-    count [S,R]; dense: kv_len [S,R] local lengths.  Returns (out [S,R,H,512] fp32, lse [S,R,H])."""
+    count [S,R]; dense: kv_len [S,R] local lengths and max_kv_len >= all of them.
+    Returns (out [S,R,H,512] fp32, lse [S,R,H])."""
     R, H, _ = q.shape
     if out is None:
         out = torch.empty((num_shards, R, H, 512), dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty((num_shards, R, H), dtype=torch.float32, device=q.device)
     a = _decode_args(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx, count, kv_len,
-                     max_kv_len, out, lse, num_splits, checked, err_flag)
-    _bind_ws(a, num_shards, False, q.device, workspace)
-    _check(load().mla_decode_partial_lse(ctypes.byref(a), num_shards, _stream(stream)),
-           "mla_decode_partial_lse")
+                     max_kv_len, out, lse, num_splits, checked, err_flag, kernel_path)
+    st = _stream(stream, q.device)
+    _bind_ws(a, num_shards, False, q.device, workspace, st)
+    _check(load().mla_decode_partial_lse(ctypes.byref(a), num_shards, st), "mla_decode_partial_lse")
     return out, lse
 
 
 def mla_decode_dcp_fused(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, dcp, interleave, *,
                          idx=None, kv_len=None, max_kv_len=None, out=None, lse=None,
-                         workspace=None, num_splits=0, checked=False, err_flag=None, stream=None):
+                         workspace=None, num_splits=0, checked=False, err_flag=None,
+                         kernel_path=DCP_PATH_AUTO, stream=None):
     """All shards of every row in one launch.  block_table [D,B,maxp]; sparse: idx [R,K] global
-    slots (-1 pad); dense: kv_len [R] global lengths.  Returns (out [R,H,512] bf16, lse [R,H])."""
+    slots (-1 pad); dense: kv_len [R] global lengths and max_kv_len >= all of them.
+    Returns (out [R,H,512] bf16, lse [R,H])."""
     R, H, _ = q.shape
     if out is None:
         out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
     a = _decode_args(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx, None, kv_len,
-                     max_kv_len, out, lse, num_splits, checked, err_flag)
-    _bind_ws(a, dcp, True, q.device, workspace)
-    _check(load().mla_decode_dcp_fused(ctypes.byref(a), dcp, interleave, _stream(stream)),
-           "mla_decode_dcp_fused")
+                     max_kv_len, out, lse, num_splits, checked, err_flag, kernel_path)
+    st = _stream(stream, q.device)
+    _bind_ws(a, dcp, True, q.device, workspace, st)
+    _check(load().mla_decode_dcp_fused(ctypes.byref(a), dcp, interleave, st), "mla_decode_dcp_fused")
     return out, lse
 
 
@@ -403,11 +421,11 @@ def mla_prefill_chunk_dcp(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, 
     need = load().mla_prefill_chunk_workspace_size(ctypes.byref(a), dcp, interleave)
     if need == ctypes.c_size_t(-1).value:
         raise DcpError(DCP_ERR_INVALID_ARG, "mla_prefill_chunk_workspace_size")
-    ws = workspace if workspace is not None else _workspace(need, q.device)
+    st = _stream(stream, q.device)
+    ws = workspace if workspace is not None else _workspace(need, q.device, st)
     a.workspace = _ptr(ws).value
     a.workspace_bytes = ws.numel() * ws.element_size()
-    _check(load().mla_prefill_chunk_dcp(ctypes.byref(a), dcp, interleave, _stream(stream)),
-           "mla_prefill_chunk_dcp")
+    _check(load().mla_prefill_chunk_dcp(ctypes.byref(a), dcp, interleave, st), "mla_prefill_chunk_dcp")
     return out, lse
 
 
@@ -426,6 +444,7 @@ def mla_decode_dcp_fused_noalloc(q, kv_pool, kv_dtype, block_table, row_seq, sm_
         raise ValueError("dense calls must pass max_kv_len (reading it from kv_len would sync)")
     a = _decode_args(q, kv_pool, kv_dtype, block_table, row_seq, sm_scale, idx, None, kv_len,
                      max_kv_len, out, lse, num_splits, checked, err_flag)
-    _check(load().mla_decode_dcp_fused_noalloc(ctypes.byref(a), dcp, interleave, _stream(stream)),
+    _check(load().mla_decode_dcp_fused_noalloc(ctypes.byref(a), dcp, interleave,
+                                               _stream(stream, q.device)),
            "mla_decode_dcp_fused_noalloc (static scratch %d bytes)" % DCP_NOALLOC_SCRATCH_BYTES)
     return out, lse

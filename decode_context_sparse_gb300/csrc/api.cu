@@ -47,6 +47,8 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
     if (a->kv_len == nullptr || a->max_kv_len < 0) return DCP_ERR_INVALID_ARG;
   }
   if (a->num_splits < 0) return DCP_ERR_INVALID_ARG;
+  if (a->kernel_path != DCP_PATH_AUTO && a->kernel_path != DCP_PATH_CUDA_CORES)
+    return DCP_ERR_INVALID_ARG;
   const int64_t units = fused ? a->rows : a->rows * n;
   const int64_t max_tokens = sparse ? a->k : a->max_kv_len;
   int splits = a->num_splits > 0 ? a->num_splits : simt_auto_splits(units, a->heads, max_tokens);
@@ -79,7 +81,8 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   p.err = a->checked ? a->err_flag : nullptr;
   // tensor-core path for 48..128 heads (rows of up to 128 heads, padded)
   // (the tensor-core path addresses pool rows with 32-bit gather coordinates)
-  p.use_tc = (tc_path_enabled() && a->heads > 32 && a->num_pages <= (int64_t)(INT32_MAX / 64)) ? 1 : 0;
+  p.use_tc = (a->kernel_path == DCP_PATH_AUTO && a->heads > 32 &&
+              a->num_pages <= (int64_t)(INT32_MAX / 64)) ? 1 : 0;
   p.pairs = 0;
   p.tc_o = p.tc_l = nullptr;
   p.tc_desc = nullptr;
@@ -95,15 +98,16 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
 
 namespace {
 
-// Binds the caller's workspace and clears the split tickets with an asynchronous memset on
-// the call's stream, so a workspace may be shared by calls of different shapes.
+// Binds the caller's workspace.  The tensor-core decode writes every split descriptor it
+// later reads; the CUDA-core path's split tickets are cleared with an asynchronous memset
+// on the call's stream.  Either way a workspace may be shared by calls of different shapes.
 int bind_workspace(const dcp_mla_decode_args* a, DecodeParams& p, cudaStream_t st) {
   if (p.use_tc) {
     const size_t need = tc_workspace_bytes(p.num_units, p.pairs);
     if (a->workspace == nullptr || a->workspace_bytes < need || !aligned(a->workspace, 256))
       return DCP_ERR_WORKSPACE;
     tc_bind_workspace(p, a->workspace);
-    return status_of(cudaMemsetAsync(p.tc_desc, 0, tc_clear_bytes(p.pairs), st));
+    return DCP_OK;
   }
   const size_t need = simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
   if (need == 0) return DCP_OK;

@@ -356,13 +356,8 @@ int simt_auto_splits(int64_t units, int heads, int64_t max_tokens) {
 template <int KVT, bool FUSED, bool SPARSE>
 static cudaError_t launch_one(const DecodeParams& p, cudaStream_t st) {
   const size_t smem = (size_t)(kHG * kDqk + kTile * kKStride) * sizeof(float);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<KVT, FUSED, SPARSE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  cudaError_t e = raise_smem_limit((const void*)decode_simt_kernel<KVT, FUSED, SPARSE>, smem);
+  if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)p.num_units, (unsigned)p.num_splits, (unsigned)(p.heads / kHG));
   decode_simt_kernel<KVT, FUSED, SPARSE><<<grid, kSimtThreads, smem, st>>>(p);
   return cudaGetLastError();

@@ -332,6 +332,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       }
     }
   }
+  // this pair's split descriptors start empty in every call (a descriptor is filled below
+  // only when the pair's range cuts a unit), so the workspace needs no clearing between calls
+  if (crank == 0 && tid == 0) {
+    p.tc_desc[2 + (int64_t)pair * 6 + 2] = 0;
+    p.tc_desc[2 + (int64_t)pair * 6 + 5] = 0;
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // peers' barriers are initialised before any remote arrive or copy
@@ -1070,12 +1076,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
 // ------------------------------------------------------------------ host side
 static size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t tc_clear_bytes(int pairs);
+size_t tc_desc_bytes(int pairs);
 
 size_t tc_workspace_bytes(int64_t units, int pairs) {
   (void)units;
   return a256((size_t)pairs * 2 * 128 * kDv * sizeof(float)) +
-         a256((size_t)pairs * 2 * 2 * 128 * sizeof(float)) + a256(tc_clear_bytes(pairs));
+         a256((size_t)pairs * 2 * 2 * 128 * sizeof(float)) + a256(tc_desc_bytes(pairs));
 }
 
 void tc_bind_workspace(DecodeParams& p, void* ws) {
@@ -1088,8 +1094,9 @@ void tc_bind_workspace(DecodeParams& p, void* ws) {
 }
 
 // Tile-sequence header (T, pairs owning tiles) and one descriptor (unit, first tile, end
-// tile) per (pair, slot), cleared before every call.
-size_t tc_clear_bytes(int pairs) { return (2 + (size_t)pairs * 2 * 3) * sizeof(int64_t); }
+// tile) per (pair, slot), all written by every decode launch (an unused descriptor gets end
+// tile 0), so nothing needs clearing between calls.
+size_t tc_desc_bytes(int pairs) { return (2 + (size_t)pairs * 2 * 3) * sizeof(int64_t); }
 
 // Merges the parts of units that several pairs' ranges cut.  One CTA per (descriptor,
 // CTA half, 16-column chunk) and one thread per head: a descriptor is merged by its pair
@@ -1159,13 +1166,7 @@ __global__ void __launch_bounds__(128) tc_split_merge_kernel(const DecodeParams 
 }
 
 int tc_pairs_for(int64_t units, int64_t tiles_bound) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 148;
-  }
+  const int sms = device_sm_count();
   // at least kMinTilesPerPair tiles per pair: a pair's set-up and pipeline fill cost about as
   // much as a dozen tiles, and a row cut between pairs adds a split merge (on 16 rows of 16
   // tiles, 76 pairs of ~3 tiles take 44 us a call, 16 pairs of one row each 31 us)
@@ -1179,12 +1180,6 @@ int tc_pairs_for(int64_t units, int64_t tiles_bound) {
 int tc_tile_slots(int kv_dtype) {
   (void)kv_dtype;
   return kTN;
-}
-
-// DCPMLA_PATH=simt selects the CUDA-core path for every head count (read at each call).
-bool tc_path_enabled() {
-  const char* e = getenv("DCPMLA_PATH");
-  return !(e && e[0] == 's');
 }
 
 // The pool as a 2-D tensor [num_pages * 64 rows][row elements] for the 4-row gathers:
@@ -1237,14 +1232,10 @@ template <int KVT, bool FUSED, bool SPARSE>
 static cudaError_t tc_launch_one(const DecodeParams& p, cudaStream_t st) {
   auto kern = decode_tc_kernel<KVT, FUSED, SPARSE>;
   const int smem = TcLay<KVT>::SMEM;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = raise_smem_limit((const void*)kern, smem);
+  if (e != cudaSuccess) return e;
   alignas(64) CUtensorMap lat, tail;
-  cudaError_t e = make_pool_maps(p, KVT, &lat, &tail);
+  e = make_pool_maps(p, KVT, &lat, &tail);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * p.pairs, 1, 1);

@@ -44,6 +44,11 @@ struct DecodeParams {
   int32_t* err_timeout;   // error word for bounded-wait timeouts (whenever given)
 };
 
+// Per-device facts (csrc/device.cu): the SM count of the current device, and raising a
+// kernel's dynamic shared-memory limit once per (device, kernel).
+int device_sm_count();
+cudaError_t raise_smem_limit(const void* kernel, size_t bytes);
+
 cudaError_t launch_remap_topk(const int32_t* gidx, int64_t rows, int k, int D, int I, int shard,
                               int32_t* local_idx, int32_t* count, cudaStream_t st);
 cudaError_t launch_local_lengths(const int32_t* glen, int64_t rows, int D, int I, int shard,
@@ -84,11 +89,10 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int kv_dtype, bool fused, 
 
 // Tensor-core decode (48..128 heads, page size 64).
 size_t tc_workspace_bytes(int64_t units, int pairs);
-size_t tc_clear_bytes(int pairs);
+size_t tc_desc_bytes(int pairs);
 void tc_bind_workspace(DecodeParams& p, void* ws);
 int tc_pairs_for(int64_t units, int64_t tiles_bound);
 int tc_tile_slots(int kv_dtype);
-bool tc_path_enabled();
 cudaError_t launch_decode_tc(const DecodeParams& p, int kv_dtype, bool fused, bool sparse,
                              cudaStream_t st);
 

@@ -134,13 +134,7 @@ cudaError_t launch_kv_write(const void* kv, int64_t n, const int32_t* seq, const
                             int D, int I, int shard, void* pool, int64_t num_pages, int kv_dtype,
                             const int32_t* bt, int num_seqs, int bt_stride, int32_t* err,
                             cudaStream_t st) {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 148;
-  }
+  const int sms = device_sm_count();
   const int64_t need = (n + kKvwRowsPerCta - 1) / kKvwRowsPerCta;
   const int grid = (int)(need < (int64_t)sms * 16 ? need : (int64_t)sms * 16);
   const uint4* k4 = static_cast<const uint4*>(kv);

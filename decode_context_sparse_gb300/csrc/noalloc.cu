@@ -55,8 +55,14 @@ extern "C" int mla_decode_dcp_fused_noalloc(const dcp_mla_decode_args* args, int
   bool sparse;
   int rc = prepare_decode(args, 1, true, dcp, interleave, p, sparse);
   if (rc != DCP_OK) return rc;
+  const size_t cap = (size_t)DCP_NOALLOC_SCRATCH_BYTES;
+  // a split count the library chose itself is lowered until its scratch fits the array (one
+  // split needs none); only a count the caller asked for is rejected when it does not fit
+  if (args->num_splits == 0)
+    while (p.num_splits > 1 && simt_workspace_bytes(p.num_units, p.heads, p.num_splits) > cap)
+      --p.num_splits;
   const size_t need = simt_workspace_bytes(p.num_units, p.heads, p.num_splits);
-  if (need > (size_t)DCP_NOALLOC_SCRATCH_BYTES) return DCP_ERR_WORKSPACE;
+  if (need > cap) return DCP_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (need > 0) {
     void* base = nullptr;

@@ -25,7 +25,6 @@
 
 namespace dcp {
 
-constexpr int kTkMaxDevices = 64;
 constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkBins = 2048;
@@ -498,17 +497,8 @@ size_t tk_smem_bytes(int stage, int kp) { return (size_t)(kTkBins + stage + kp) 
 template <bool MERGE>
 cudaError_t tk_launch(const TopkParams& p, int64_t lists, cudaStream_t st) {
   const size_t smem = tk_smem_bytes(p.stage, MERGE ? 2 * p.kp : 0);  // merge: two run buffers
-  // raise the kernel's dynamic shared-memory limit once per device and size
-  static int allowed[kTkMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = raise_smem_limit((const void*)topk_kernel<MERGE>, smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kTkMaxDevices || (size_t)allowed[dev] < smem) {
-    e = cudaFuncSetAttribute(topk_kernel<MERGE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kTkMaxDevices) allowed[dev] = (int)smem;
-  }
   topk_kernel<MERGE><<<(unsigned)lists, kTkThreads, smem, st>>>(p);
   return cudaGetLastError();
 }

@@ -68,7 +68,7 @@ typedef enum {
 const char* dcp_status_string(int status);
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define DCP_ABI_VERSION 1
+#define DCP_ABI_VERSION 2
 int dcp_abi_version(void);
 
 /*
@@ -231,15 +231,26 @@ typedef struct {
   /* scratch */
   void* workspace;             /* (device) >= mla_decode_workspace_size() bytes, 256-B
                                   aligned; its contents need not persist between calls
-                                  (a call clears what it uses with an asynchronous
-                                  memset on its stream).  Calls that share a workspace
-                                  must not overlap on the GPU. */
+                                  and need no initialisation (the tensor-core kernel
+                                  writes everything it reads; the CUDA-core kernel clears
+                                  its tickets with an asynchronous memset on the stream).
+                                  Calls that share a workspace must not overlap on the
+                                  GPU. */
   size_t workspace_bytes;
   int32_t num_splits;          /* split-KV factor per row: 0 = library choice */
   /* diagnostics */
   int32_t checked;             /* != 0: bounds-check every slot and page id */
   int32_t* err_flag;           /* (device, optional) DCP_ERRBIT_* ORed in when checked */
+  /* kernel choice: DCP_PATH_AUTO or DCP_PATH_CUDA_CORES; the workspace size query must
+   * see the same value as the call */
+  int32_t kernel_path;
 } dcp_mla_decode_args;
+
+/* Values of dcp_mla_decode_args.kernel_path.  AUTO: the tensor-core kernel for 48..128
+ * heads, the CUDA-core kernel otherwise.  CUDA_CORES: the CUDA-core kernel for every head
+ * count (same results within the tolerances; slower; for comparing the two kernels). */
+#define DCP_PATH_AUTO 0
+#define DCP_PATH_CUDA_CORES 1
 
 /*
  * mla_decode_partial_lse -- MLA decode attention over one or more shards' local KV,
@@ -306,9 +317,13 @@ int mla_decode_dcp_fused(const dcp_mla_decode_args* args, int32_t dcp, int32_t i
  * the process exits.  The call allocates and frees nothing.
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
- *   - A call whose split-KV scratch would exceed DCP_NOALLOC_SCRATCH_BYTES
- *     (rows * splits * heads * 2 KB plus small tables) returns DCP_ERR_WORKSPACE and
- *     launches nothing; lower num_splits or the rows per call.
+ *   - It runs the CUDA-core split-KV kernel for every head count (args->kernel_path is
+ *     ignored): the tensor-core kernel's scratch (about 0.5 MB per pair of SMs) does not
+ *     fit the array.  For 128 heads it is many times slower than mla_decode_dcp_fused.
+ *   - With num_splits = 0 the library lowers its split count until the scratch
+ *     (rows * splits * heads * 2 KB plus small tables) fits the array.  A call whose
+ *     requested num_splits needs more returns DCP_ERR_WORKSPACE and launches nothing;
+ *     lower num_splits or the rows per call.
  *   - All calls share the array and it keeps the last call's contents; each call clears
  *     the tickets it needs with an asynchronous memset on its stream.  Calls that overlap
  *     on the GPU (different streams or host threads) race on the array.

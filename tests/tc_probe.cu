@@ -186,87 +186,3 @@ extern "C" int wait_timeout_probe(int* out) {
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
-// Where an M = 64 MMA (kind::f16, one CTA, N = 64, A and B K-major in shared memory) puts
-// D[m][n] in TMEM: inputs make D[m][n] = (m + 1) + 256 (n + 1) exactly; TMEM columns
-// [0, 256) of all 128 lanes are zeroed first and read back into out[128][256].
-__global__ void __launch_bounds__(128) m64_layout_kernel(float* out, int* err) {
-  extern __shared__ unsigned char sm_raw[];
-  unsigned char* sm = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
-  unsigned char* sA = sm;         // 64 rows x 64 K bf16, SW128 K-major
-  unsigned char* sB = sm + 8192;  // 64 rows x 64 K bf16
-  __shared__ uint64_t bar;
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if (warp == 0) {
-    tmem_alloc(&tmem_base, 512);
-    tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  // A[m][0] = m + 1, A[m][1] = 1; B[n][0] = 1, B[n][1] = 256 (n + 1); zeros elsewhere
-  for (int i = tid; i < 64 * 8; i += 128) {
-    const int r = i / 8, c = i % 8;
-    uint32_t a01 = 0u, b01 = 0u;
-    if (c == 0) {
-      const uint32_t am = __float_as_uint((float)(r + 1)) >> 16;  // exact in bf16
-      const uint32_t one = __float_as_uint(1.0f) >> 16;
-      const uint32_t bn = __float_as_uint(256.0f * (r + 1)) >> 16;
-      a01 = am | (one << 16);
-      b01 = one | (bn << 16);
-    }
-    *reinterpret_cast<uint4*>(sA + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(a01, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(sB + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(b01, 0u, 0u, 0u);
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = tmem_base;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  {
-    uint32_t z[16] = {0u};
-    for (int c = 0; c < 256; c += 16) tmem_st16(tbase + lane_off + c, z);
-    tmem_st_wait();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (tid == 0) {
-    const uint32_t idesc = idesc_bf16(64, 64, 0, 0);
-    for (int ks = 0; ks < 4; ++ks)
-      mma_ss(tbase, smem_desc(smem_u32(sA) + ks * 32, 16, 1024),
-             smem_desc(smem_u32(sB) + ks * 32, 16, 1024), idesc, ks > 0);
-    mma_commit(&bar);
-  }
-  __syncwarp();
-  const bool ok = mbar_wait(&bar, 0, &abort_flag);
-  tc_fence_after();
-  if (!ok) {
-    if (tid == 0) atomicOr(err, 1);
-  } else {
-    for (int c = 0; c < 256; c += 16) {
-      uint32_t r[16];
-      tmem_ld16(tbase + lane_off + c, r);
-      tmem_ld_wait();
-      for (int i = 0; i < 16; ++i) out[tid * 256 + c + i] = __uint_as_float(r[i]);
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 512);
-}
-
-extern "C" int m64_layout_probe(float* out, int* err) {
-  const int smem = 16384 + 1024;
-  if (cudaFuncSetAttribute(m64_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return -3;
-  m64_layout_kernel<<<1, 128, smem>>>(out, err);
-  return cudaGetLastError() == cudaSuccess ? 0 : -3;
-}
-

@@ -184,3 +184,39 @@ def test_prefill_chunk_entry_checks(lib):
     assert lib.mla_prefill_chunk_dcp(R(_args(max_kv_len=5000)), 8, 1, None) == E   # no prefix lengths
     assert lib.mla_prefill_chunk_dcp(R(_args(idx=None, **good)), 8, 1, None) == E   # no chunk slots
     assert lib.mla_prefill_chunk_dcp(R(_args(**good)), 8, 0, None) == E            # interleave 0
+
+
+def test_kernel_path_field(lib):
+    import decode_context_sparse_gb300 as dcp
+    R = ctypes.byref
+    # an unknown kernel choice is refused before any launch
+    assert lib.mla_decode_dcp_fused(R(_args(kernel_path=7)), 8, 1, None) == dcp.DCP_ERR_INVALID_ARG
+    assert lib.mla_decode_workspace_size(R(_args(kernel_path=-1)), 8, 1) == ctypes.c_size_t(-1).value
+    # the field is read: with 128 heads and one split the CUDA-core kernel needs no workspace,
+    # the tensor-core kernel (the automatic choice) does
+    assert lib.mla_decode_workspace_size(R(_args(num_splits=1, kernel_path=dcp.DCP_PATH_CUDA_CORES)),
+                                         8, 1) == 0
+    assert lib.mla_decode_workspace_size(R(_args(num_splits=1, kernel_path=dcp.DCP_PATH_AUTO)),
+                                         8, 1) > 0
+
+
+def test_args_struct_layout_matches_header(tmp_path):
+    """The binding's ctypes mirror of dcp_mla_decode_args has the C compiler's layout: a tiny C
+    program built against include/dcpmla.h prints every field's offset and the size."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    import decode_context_sparse_gb300 as dcp
+    names = [f[0] for f in dcp.DecodeArgs._fields_]
+    src = tmp_path / "layout.c"
+    body = "".join('  printf("%%s %%zu\\n", "%s", offsetof(dcp_mla_decode_args, %s));\n' % (n, n)
+                   for n in names)
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "dcpmla.h"\nint main(void) {\n'
+                   + body + '  printf("sizeof %zu\\n", sizeof(dcp_mla_decode_args));\n  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = dict(line.split() for line in subprocess.check_output([str(exe)]).decode().splitlines())
+    for n in names:
+        assert int(got[n]) == getattr(dcp.DecodeArgs, n).offset, n
+    assert int(got["sizeof"]) == ctypes.sizeof(dcp.DecodeArgs)

@@ -1,14 +1,13 @@
-"""Both decode paths through the C ABI: the tensor-core path (taken for 48..128 heads) and
-the CUDA-core path (taken for fewer heads, or for any head count with DCPMLA_PATH=simt)
-agree with the oracle on the same inputs, including rows cut across CTA pairs."""
-import os
-
+"""Both decode kernels through the C ABI: the tensor-core kernel (taken for 48..128 heads)
+and the CUDA-core kernel (taken for fewer heads, or for any head count when a call sets
+kernel_path = DCP_PATH_CUDA_CORES) agree with the oracle on the same inputs, including rows
+cut across CTA pairs."""
 import pytest
 import torch
 
 import oracle
 import synth
-from parity import check_lse, check_out, run_fused, run_unfused
+from parity import check_lse, check_out, run_fused
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -25,22 +24,21 @@ def dcp():
     return m
 
 
-@pytest.mark.parametrize("path", ["simt", "tc"])
+@pytest.mark.parametrize("path", ["cuda_cores", "auto"])
 @pytest.mark.parametrize("kv", [synth.KV_BF16, synth.KV_FP8])
 def test_both_paths_match_oracle(dcp, path, kv):
+    kp = dcp.DCP_PATH_CUDA_CORES if path == "cuda_cores" else dcp.DCP_PATH_AUTO
     prob = synth.make_decode_problem("paths", [3100, 1700], 128, 1000, kv, 4, 1, mtp=3, seed=81)
-    old = os.environ.get("DCPMLA_PATH")
-    os.environ["DCPMLA_PATH"] = path
-    try:
-        g = prob.to(DEV)
-        po, pl, mo, ml = run_unfused(dcp, g)
-        fo, fl = run_fused(dcp, g)
-        torch.cuda.synchronize()
-    finally:
-        if old is None:
-            del os.environ["DCPMLA_PATH"]
-        else:
-            os.environ["DCPMLA_PATH"] = old
+    g = prob.to(DEV)
+    D = g.dcp
+    loc, cnt = dcp.dcp_remap_topk(g.topk, D, g.interleave)
+    po, pl = dcp.mla_decode_partial_lse(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq,
+                                        g.sm_scale, idx=loc, count=cnt, num_shards=D,
+                                        kernel_path=kp)
+    mo, ml = dcp.dcp_lse_merge(po, pl)
+    fo, fl = dcp.mla_decode_dcp_fused(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq,
+                                      g.sm_scale, D, g.interleave, idx=g.topk, kernel_path=kp)
+    torch.cuda.synchronize()
     ro, rl = oracle.attention_problem(prob)
     check_out(fo, ro, path + " fused out")
     check_lse(fl, rl, path + " fused lse")
@@ -57,3 +55,24 @@ def test_tc_timeout_flag_stays_clear(dcp):
     run_fused(dcp, prob, err_flag=err)
     torch.cuda.synchronize()
     assert err.item() == 0
+
+
+@pytest.mark.parametrize("path", ["cuda_cores", "auto"])
+def test_second_device_after_first(dcp, path):
+    """Per-device launch set-up: a decode on cuda:1 after one on cuda:0 in the same process
+    (the shared-memory limit of each kernel and the SM count are per device).  Needs two
+    visible GPUs."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two GPUs")
+    kp = dcp.DCP_PATH_CUDA_CORES if path == "cuda_cores" else dcp.DCP_PATH_AUTO
+    prob = synth.make_decode_problem("dev2", [2000, 900], 128, 512, synth.KV_FP8, 4, 1, mtp=2, seed=83)
+    ro, rl = oracle.attention_problem(prob)
+    for dev in ("cuda:0", "cuda:1"):
+        with torch.cuda.device(dev):
+            g = prob.to(dev)
+            fo, fl = dcp.mla_decode_dcp_fused(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq,
+                                              g.sm_scale, g.dcp, g.interleave, idx=g.topk,
+                                              kernel_path=kp)
+            torch.cuda.synchronize()
+        check_out(fo, ro, "%s %s fused out" % (dev, path))
+        check_lse(fl, rl, "%s %s fused lse" % (dev, path))

@@ -26,7 +26,6 @@ def probe():
     lib.e4m3_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     lib.e4m3x4_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     lib.wait_timeout_probe.argtypes = [ctypes.c_void_p]
-    lib.m64_layout_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     return lib
 
 
@@ -96,22 +95,3 @@ def test_bounded_wait_gives_up_and_reports(probe):
     assert 900 <= ms <= 10000, ms
     assert (torch.ones(4, device="cuda") * 2).sum().item() == 8.0
 
-
-def test_m64_mma_tmem_layout(probe):
-    """An M = 64 MMA (one CTA, kind::f16, N = 64) writes row m of its result to TMEM lane
-    32 * (m // 16) + m % 16, column n: the first 16 lanes of each 32-lane sub-partition;
-    the other lanes are not written."""
-    out = torch.zeros(128 * 256, dtype=torch.float32, device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    assert probe.m64_layout_probe(out.data_ptr(), err.data_ptr()) == 0
-    torch.cuda.synchronize()
-    assert err.item() == 0
-    o = out.cpu().view(128, 256)
-    m = torch.arange(64).view(64, 1)
-    n = torch.arange(64).view(1, 64)
-    lanes = 32 * (m // 16) + m % 16
-    want = ((m + 1) + 256 * (n + 1)).float()
-    assert torch.equal(o[lanes.expand(64, 64), n.expand(64, 64)], want)
-    mask = torch.ones(128, 256, dtype=torch.bool)
-    mask[lanes.expand(64, 64), n.expand(64, 64)] = False
-    assert bool((o[mask] == 0).all())

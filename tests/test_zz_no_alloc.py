@@ -70,3 +70,12 @@ def test_noalloc_rejects_scratch_beyond_the_limit(dcp):
                                          prob.row_seq, prob.sm_scale, prob.dcp, prob.interleave,
                                          out=out, lse=lse, idx=prob.topk, num_splits=64)
     assert e.value.status == dcp.DCP_ERR_WORKSPACE
+
+
+def test_noalloc_auto_splits_fit_the_static_scratch(dcp):
+    """A short dense call with long contexts: the library's own split choice would need more
+    than the static scratch; with num_splits = 0 it lowers the split count instead of
+    refusing the call."""
+    prob = synth.make_decode_problem("noalloc_long", [65536, 60000], 128, None, synth.KV_BF16, 2,
+                                     1, seed=74).to(DEV)
+    _compare_two_calls(dcp, prob, kv_len=prob.row_len, max_kv_len=65536)
