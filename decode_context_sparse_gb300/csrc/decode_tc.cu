@@ -85,7 +85,6 @@ constexpr int kTcThreads = 640;
 constexpr int kMinTilesPerPair = 16;
 constexpr int kColO = 0, kColQ = 256, kColS = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kScaleFloor = 8.67361737988403547e-19f;  // 2^-60
 
 template <int KVT>
 struct TcLay {
@@ -217,6 +216,28 @@ __device__ __forceinline__ int64_t block_scan_excl(int64_t v, int64_t* warp_sum,
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&t);
+}
+
+// FP8 block scale s = m * 2^E with E = floor(log2 s) clamped to at most 7 (so that codes *
+// 2^E, |code| <= 448, stay finite in FP16) and m = s / 2^E, in [1, 2) unless E was clamped.
+// A block whose scale is 0, or below 2^-24 (its values below 448 * 2^-24 in magnitude),
+// counts as zero: multiplier 0, m 0.
+__device__ __forceinline__ int fp8_block_exp(float s) {
+  const int e = (int)((__float_as_uint(s) >> 23) & 0xFF) - 127;
+  return e > 7 ? 7 : e;
+}
+__device__ __forceinline__ float fp8_block_m(float s) {
+  const int e = fp8_block_exp(s);
+  if (!(s > 0.f) || e < -24) return 0.f;
+  return s * __uint_as_float((uint32_t)(127 - e) << 23);  // s * 2^-e, exact
+}
+// f16x2 holding 2^E twice (the codes' multiplier), or 0.
+__device__ __forceinline__ uint32_t fp8_block_mul(float s) {
+  const int e = fp8_block_exp(s);
+  if (!(s > 0.f) || e < -24) return 0u;
+  // 2^e as FP16: normal for e >= -14 (biased exponent e + 15), subnormal below
+  const uint32_t h = e >= -14 ? (uint32_t)(e + 15) << 10 : (uint32_t)1 << (e + 24);
+  return h | (h << 16);
 }
 
 template <int KVT, bool FUSED, bool SPARSE>
@@ -472,8 +493,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     //   QK(jq): Q of its unit in TMEM (q_ready; the pair's first tile always loads Q), K tile
     //           jq converted (kt_full), logit buffer jq&1 read by stage A(jq-2) (s_free);
     //   PV(jp): P(jp) in shared memory (p_full).
-    constexpr uint32_t idesc_qk = idesc_bf16(128, TN, 0, 0);
-    constexpr uint32_t idesc_pv = FP8 ? idesc_bf16(128, 128, 0, 1) : idesc_bf16(128, 256, 0, 1);
+    constexpr uint32_t idesc_qk = idesc_f16(128, TN, 0, 0);
+    constexpr uint32_t idesc_pv = FP8 ? idesc_f16(128, 128, 0, 1) : idesc_f16(128, 256, 0, 1);
     const uint32_t qb = tbase + kColQ;
     const uint64_t qrd = smem_desc(smem_u32(smem + L::OFF_QR), 16, 1024);
     const uint32_t leader = elect_one();
@@ -574,6 +595,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     // Latent part: thread -> slot t = 8*(warp-4) + 2*(lane>>3) + ((lane>>2)&1), 16-B chunks
     // ch = (lane&3) + 4*(it ^ ((lane>>2)&1)): each 8-lane phase of a 16-B access reads 8
     // distinct bank groups of the staging rows and writes 8 distinct swizzled chunks.
+    // The K tile holds FP16 values.  FP8: a block's codes times 2^E, E the power-of-two part
+    // of the block's scale (exact in FP16), the rest m = scale / 2^E in [1, 2) kept for the
+    // logit and P; BF16: the values themselves.
     const int ct = tid - 128;
     const int l8 = lane & 7, hb = l8 >> 2;
     const int t = 8 * (ct >> 5) + 2 * (lane >> 3) + hb;
@@ -589,6 +613,14 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
       const bool live = (mask >> t) & 1;
       if (FP8) {
+        // this slot's two block scales -> f16x2 multipliers 2^E (0 for a negligible block)
+        float2 sc = make_float2(0.f, 0.f);
+        if (live) {
+          const float* sp = reinterpret_cast<const float*>(
+              stg + L::STG_TAIL + (t >> 2) * C::TAIL_GSTRIDE + (t & 3) * C::TAIL_TOK);
+          sc = make_float2(sp[2 * crank], sp[2 * crank + 1]);
+        }
+        const uint32_t mul2[2] = {fp8_block_mul(sc.x), fp8_block_mul(sc.y)};
         uint4 v[4];
 #pragma unroll
         for (int it = 0; it < 4; ++it) {  // 16 codes per chunk
@@ -598,13 +630,13 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int ch = (l8 & 3) + 4 * (it ^ hb);
+          const uint32_t mul = mul2[ch >> 3];
           const uint32_t in[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
           uint32_t o[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const uint2 w = e4m3x4_to_bf16x4(in[e]);
-            o[2 * e] = w.x;
-            o[2 * e + 1] = w.y;
+            o[2 * e] = e4m3x2_to_f16x2_mul((uint16_t)(in[e] & 0xffffu), mul);
+            o[2 * e + 1] = e4m3x2_to_f16x2_mul((uint16_t)(in[e] >> 16), mul);
           }
           unsigned char* base = kt + (ch >> 2) * L::BS + t * 128;
           const int c16 = (ch & 3) * 2;
@@ -612,26 +644,29 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           *reinterpret_cast<uint4*>(base + (((c16 + 1) ^ (t & 7)) << 4)) =
               make_uint4(o[4], o[5], o[6], o[7]);
         }
-        {  // RoPE: thread -> (slot rt, 8 of this CTA's 32 dims); scales
+        {  // RoPE: thread -> (slot rt, 8 of this CTA's 32 dims); block multipliers
           const int rt = ct >> 2, c4 = ct & 3;
           const unsigned char* tail = stg + L::STG_TAIL + (rt >> 2) * C::TAIL_GSTRIDE + (rt & 3) * C::TAIL_TOK;
           uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
-          float slo = 0.f, shi = 0.f, sf = 1.f;
+          float mlo = 0.f, mhi = 0.f, mf = 1.f;
           if ((mask >> rt) & 1) {
-            const float4 sc = *reinterpret_cast<const float4*>(tail);
-            slo = crank == 0 ? sc.x : sc.z;
-            shi = crank == 0 ? sc.y : sc.w;
-            sf = fabsf(slo) < kScaleFloor ? kScaleFloor : slo;
-            const float inv = 1.0f / sf;
+            const float4 sc4 = *reinterpret_cast<const float4*>(tail);
+            mlo = fp8_block_m(crank == 0 ? sc4.x : sc4.z);
+            mhi = fp8_block_m(crank == 0 ? sc4.y : sc4.w);
+            // the RoPE part rides in the lo accumulator, which is scaled by m_lo later;
+            // m_lo is 0 only for a block whose values are all zero (its codes count as 0)
+            mf = mlo > 0.f ? mlo : 1.f;
+            const float inv = 1.0f / mf;
             const uint4 r = *reinterpret_cast<const uint4*>(tail + 16 + 64 * crank + 16 * c4);
             const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float y0 = __uint_as_float(rw[e] << 16) * inv;
               const float y1 = __uint_as_float(rw[e] & 0xffff0000u) * inv;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(y0, y1);
-              hw[e] = *reinterpret_cast<const uint32_t*>(&h2);
-              lw[e] = pack_bf16x2(y0 - __low2float(h2), y1 - __high2float(h2));
+              const uint32_t h2 = pack_f16x2(y0, y1);
+              const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+              hw[e] = h2;
+              lw[e] = pack_f16x2(y0 - hf.x, y1 - hf.y);
             }
           }
           unsigned char* rb = kt + 4 * L::BS + rt * 128;
@@ -639,12 +674,11 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           *reinterpret_cast<uint4*>(rb + (((4 + c4) ^ (rt & 7)) << 4)) =
               make_uint4(lw[0], lw[1], lw[2], lw[3]);
           if (c4 == 0) {
-            float* mf = reinterpret_cast<float*>(meta);
-            mf[rt] = sf * sl2;
-            mf[TN + rt] = shi * sl2;
-            __nv_bfloat16* pb = reinterpret_cast<__nv_bfloat16*>(mf + 2 * TN);
-            pb[rt] = __float2bfloat16_rn(slo);
-            pb[TN + rt] = __float2bfloat16_rn(shi);
+            float* mfp = reinterpret_cast<float*>(meta);
+            mfp[rt] = mf * sl2;        // logit multiplier of the lo accumulator
+            mfp[TN + rt] = mhi * sl2;  // of the hi accumulator
+            mfp[2 * TN + rt] = mlo;    // P multipliers of the lo / hi block values
+            mfp[3 * TN + rt] = mhi;
           }
         }
       } else {
@@ -657,13 +691,17 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
           const int ch = (l8 & 3) + 4 * (it ^ hb);
-          *reinterpret_cast<uint4*>(kt + (ch >> 3) * L::BS + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = v[it];
+          const uint4 w = make_uint4(bf16x2_to_f16x2_mul(v[it].x, 1.f), bf16x2_to_f16x2_mul(v[it].y, 1.f),
+                                     bf16x2_to_f16x2_mul(v[it].z, 1.f), bf16x2_to_f16x2_mul(v[it].w, 1.f));
+          *reinterpret_cast<uint4*>(kt + (ch >> 3) * L::BS + t * 128 + (((ch & 7) ^ (t & 7)) << 4)) = w;
         }
         {
           const int rt = ct >> 2, c4 = ct & 3;
-          const uint4 r = (mask >> rt) & 1
-                              ? *reinterpret_cast<const uint4*>(stg + L::STG_TAIL + rt * C::TAIL_TOK + c4 * 16)
-                              : zero;
+          uint4 r = (mask >> rt) & 1
+                        ? *reinterpret_cast<const uint4*>(stg + L::STG_TAIL + rt * C::TAIL_TOK + c4 * 16)
+                        : zero;
+          r = make_uint4(bf16x2_to_f16x2_mul(r.x, 1.f), bf16x2_to_f16x2_mul(r.y, 1.f),
+                         bf16x2_to_f16x2_mul(r.z, 1.f), bf16x2_to_f16x2_mul(r.w, 1.f));
           *reinterpret_cast<uint4*>(kt + 4 * L::BS + rt * 128 + ((c4 ^ (rt & 7)) << 4)) = r;
         }
       }
@@ -681,18 +719,37 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     float* xin = reinterpret_cast<float*>(smem + L::OFF_X);
     float* xself = reinterpret_cast<float*>(smem + L::OFF_SELF);
-    // Q of row r: this CTA's 256 latent dims into TMEM (two bf16 per column), its 32 RoPE
-    // dims into row h of the SW128 A-operand tile in shared memory
+    // Q of row r as FP16: this CTA's 256 latent dims into TMEM (two per column), its 32 RoPE
+    // dims into row h of the SW128 A-operand tile in shared memory.  The head's values are
+    // multiplied by 2^(14 - e), e the exponent of their largest magnitude (exact; keeps them
+    // in FP16's range), and the head's logits by qs = 2^(e - 14) to undo it.
+    float qs = 1.0f;
     auto load_q = [&](int64_t r) {
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) + (r * H + h) * kDqk);
+      uint32_t mx = 0;  // largest |bf16| bit pattern over this CTA's 288 dims
+      if (h < H) {
+#pragma unroll 4
+        for (int i = 0; i < 36; ++i) {
+          const uint4 v = __ldg(src + (i < 32 ? crank * 32 + i : 64 + crank * 4 + (i - 32)));
+          const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
+                                 v.w & 0x7fff7fffu};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
+        }
+      }
+      const int e = (int)(mx >> 7) - 127;  // exponent of the largest magnitude
+      const bool zero = mx == 0 || e > 127 - 14;
+      const float up = zero ? 1.0f : __uint_as_float((uint32_t)(127 + 14 - e) << 23);
+      qs = zero ? 1.0f : __uint_as_float((uint32_t)(127 - 14 + e) << 23);
       for (int c = 0; c < 8; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (h < H) v = __ldg(src + crank * 32 + c * 4 + i);
-          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+          w[4 * i] = bf16x2_to_f16x2_mul(v.x, up); w[4 * i + 1] = bf16x2_to_f16x2_mul(v.y, up);
+          w[4 * i + 2] = bf16x2_to_f16x2_mul(v.z, up); w[4 * i + 3] = bf16x2_to_f16x2_mul(v.w, up);
         }
         tmem_st16(trow + kColQ + 16 * c, w);
       }
@@ -701,6 +758,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       for (int i = 0; i < 4; ++i) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (h < H) v = __ldg(src + 64 + crank * 4 + i);
+        v = make_uint4(bf16x2_to_f16x2_mul(v.x, up), bf16x2_to_f16x2_mul(v.y, up),
+                       bf16x2_to_f16x2_mul(v.z, up), bf16x2_to_f16x2_mul(v.w, up));
         *reinterpret_cast<uint4*>(qr + ((i ^ (h & 7)) << 4)) = v;
       }
       fence_proxy_async_smem();
@@ -721,14 +780,16 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       tc_fence_after();
       const unsigned char* meta = smem + L::OFF_META + (j % NK) * L::META_BYTES;
       const uint32_t sb = trow + kColS + buf * L::SBUF;
+      const float qs_tile = qs;  // this tile's unit (the next unit's Q may load below)
       float s[TN];
       if (!FP8) {
         uint32_t a[TN];
         tmem_ld16(sb, a);
         tmem_ld16(sb + 16, a + 16);
         tmem_ld_wait();
+        const float f = p.scale_log2 * qs_tile;
 #pragma unroll
-        for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * p.scale_log2;
+        for (int t = 0; t < TN; ++t) s[t] = __uint_as_float(a[t]) * f;
       } else {
         const float4* ma = reinterpret_cast<const float4*>(meta);
         const float4* mb = ma + TN / 4;
@@ -742,10 +803,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           for (int t4 = 0; t4 < 4; ++t4) {
             const float4 a = ma[4 * hf + t4], b = mb[4 * hf + t4];
             const int t = 16 * hf + 4 * t4;
-            s[t] = fmaf(__uint_as_float(lo[4 * t4]), a.x, __uint_as_float(hi[4 * t4]) * b.x);
-            s[t + 1] = fmaf(__uint_as_float(lo[4 * t4 + 1]), a.y, __uint_as_float(hi[4 * t4 + 1]) * b.y);
-            s[t + 2] = fmaf(__uint_as_float(lo[4 * t4 + 2]), a.z, __uint_as_float(hi[4 * t4 + 2]) * b.z);
-            s[t + 3] = fmaf(__uint_as_float(lo[4 * t4 + 3]), a.w, __uint_as_float(hi[4 * t4 + 3]) * b.w);
+            s[t] = fmaf(__uint_as_float(lo[4 * t4]), a.x, __uint_as_float(hi[4 * t4]) * b.x) * qs_tile;
+            s[t + 1] = fmaf(__uint_as_float(lo[4 * t4 + 1]), a.y, __uint_as_float(hi[4 * t4 + 1]) * b.y) * qs_tile;
+            s[t + 2] = fmaf(__uint_as_float(lo[4 * t4 + 2]), a.z, __uint_as_float(hi[4 * t4 + 2]) * b.z) * qs_tile;
+            s[t + 3] = fmaf(__uint_as_float(lo[4 * t4 + 3]), a.w, __uint_as_float(hi[4 * t4 + 3]) * b.w) * qs_tile;
           }
         }
       }
@@ -997,33 +1058,26 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           !(ok = mbar_wait(&sh.pv_done[(j - C::NP) & 1], ((j - C::NP) >> 1) & 1, abort_flag)))
         break;
       const int sw = h & 7;  // SW128: 16-B chunk c of row h sits at chunk c ^ (h & 7)
-      if (!FP8) {  // P row: 32 bf16 in chunks 0-3; this half's 16 in chunks 2*half, 2*half+1
+      if (!FP8) {  // P row: 32 fp16 in chunks 0-3; this half's 16 in chunks 2*half, 2*half+1
         uint32_t pw[TH / 2];
 #pragma unroll
-        for (int i = 0; i < TH / 2; ++i) pw[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+        for (int i = 0; i < TH / 2; ++i) pw[i] = pack_f16x2(pr[2 * i], pr[2 * i + 1]);
 #pragma unroll
         for (int c = 0; c < 2; ++c)
           *reinterpret_cast<uint4*>(prow + (((2 * half + c) ^ sw) << 4)) =
               make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
-      } else {  // P row: [p*s_lo slots 0-31 | p*s_hi slots 0-31], chunks 0-3 | 4-7
-        const uint4* pl4 = reinterpret_cast<const uint4*>(meta + 8 * TN) + 2 * half;  // bf16 s_lo
-        const uint4* ph4 = pl4 + TN / 8;                                             // bf16 s_hi
+      } else {  // P row: [p*m_lo slots 0-31 | p*m_hi slots 0-31] as fp16, chunks 0-3 | 4-7
+        const float* ml = reinterpret_cast<const float*>(meta) + 2 * TN + cb;  // m_lo of the slots
+        const float* mh = ml + TN;                                               // m_hi
         uint32_t plo[TH / 2], phi[TH / 2];
 #pragma unroll
-        for (int i = 0; i < TH / 8; ++i) {
-          const uint4 a = pl4[i], b = ph4[i];
-          const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int m = 4 * i + k;
-            const uint32_t pp = pack_bf16x2(pr[2 * m], pr[2 * m + 1]);
-            __nv_bfloat162 r1 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pp),
-                                        *reinterpret_cast<const __nv_bfloat162*>(&aw[k]));
-            __nv_bfloat162 r2 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&pp),
-                                        *reinterpret_cast<const __nv_bfloat162*>(&bw[k]));
-            plo[m] = *reinterpret_cast<uint32_t*>(&r1);
-            phi[m] = *reinterpret_cast<uint32_t*>(&r2);
-          }
+        for (int i = 0; i < TH / 4; ++i) {
+          const float4 a = reinterpret_cast<const float4*>(ml)[i];
+          const float4 b = reinterpret_cast<const float4*>(mh)[i];
+          plo[2 * i] = pack_f16x2(pr[4 * i] * a.x, pr[4 * i + 1] * a.y);
+          plo[2 * i + 1] = pack_f16x2(pr[4 * i + 2] * a.z, pr[4 * i + 3] * a.w);
+          phi[2 * i] = pack_f16x2(pr[4 * i] * b.x, pr[4 * i + 1] * b.y);
+          phi[2 * i + 1] = pack_f16x2(pr[4 * i + 2] * b.z, pr[4 * i + 3] * b.w);
         }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {

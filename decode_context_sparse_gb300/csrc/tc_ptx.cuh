@@ -190,6 +190,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16: FP16 A and B, FP32 accumulator (A/B type fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 constexpr uint32_t kLayoutSW128 = 2;
 // Shared-memory matrix descriptor (sm_100 format, version bit 46).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
@@ -356,6 +362,26 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 
 // ------------------------------------------------------------------ conversions
+// Two E4M3 codes (lower code in the lower half) -> f16x2 of the same values, exactly (every
+// E4M3 value is an FP16 value), each multiplied by the f16x2 `mul` (a power of two or 0;
+// the product is exact while it stays in FP16's normal range).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_mul(uint16_t codes, uint32_t mul) {
+  uint32_t h2, r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h2), "r"(mul));
+  return r;
+}
+// Two floats -> f16x2 (a in the lower half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+// Two bf16 (a word: lower value in the lower half) times a power of two -> f16x2.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_mul(uint32_t w, float mul) {
+  return pack_f16x2(__uint_as_float(w << 16) * mul, __uint_as_float(w & 0xffff0000u) * mul);
+}
+
 // Two E4M3 codes -> two bf16 holding value * 2^-112, exactly: the hardware E4M3 -> F16
 // conversion is exact and every non-zero E4M3 value is a normal f16 with at most three
 // mantissa bits, so shifting the f16 magnitude bits right by three re-reads them as a
