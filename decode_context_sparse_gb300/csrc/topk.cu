@@ -263,16 +263,29 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
       if (dg > 0) {
         for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
         __syncthreads();
-        for (int c = 0; c < rounds; ++c) {
-          const uint4 k4 = get4(c);
-          const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+        if (staged && !lo) {
+          // a high-word digit over the staged keys: compile-time shifts, one 16-B load per
+          // four keys, an atomic only for the keys still in play (a few per thread)
+          for (int c = 0; c < rounds; ++c) {
+            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + c * kTkRound + 4 * tid);
+            const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (!lo) {
-              hist_add(hist, h[e], msk_hi, pre_hi, shift, nb);
-            } else if (h[e] != 0u && h[e] == pre_hi) {
-              const uint32_t l = ~(uint32_t)src.gid(c * kTkRound + 4 * tid + e);
-              if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
+            for (int e = 0; e < 4; ++e)
+              if (h[e] != 0u && (h[e] & msk_hi) == pre_hi)
+                atomicAdd(&hist[dg == 1 ? (h[e] >> 10) & 2047u : h[e] & 1023u], 1u);
+          }
+        } else {
+          for (int c = 0; c < rounds; ++c) {
+            const uint4 k4 = get4(c);
+            const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (!lo) {
+                hist_add(hist, h[e], msk_hi, pre_hi, shift, nb);
+              } else if (h[e] != 0u && h[e] == pre_hi) {
+                const uint32_t l = ~(uint32_t)src.gid(c * kTkRound + 4 * tid + e);
+                if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
+              }
             }
           }
         }
@@ -296,87 +309,122 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
     t_lo = pre_lo;
   }
 
-  // stable compaction of the selected entries in index order (at most k), a block of
-  // kTkBlockRounds rounds at a time: count per (round, warp), one scan, then each warp
-  // writes its entries at positions found with ballots
   auto selected = [&](uint32_t h, int i) -> bool {
     return h != 0u && (h > t_hi || (h == t_hi && (t_lo == 0u || ~(uint32_t)src.gid(i) >= t_lo)));
   };
   const bool no_ties = t_lo == 0u;  // then the selection is key >= t_hi (t_hi >= 1)
-  auto sel4 = [&](const uint4& k4, int i) -> uint32_t {  // bit e: entry i + e is selected
-    if (no_ties)
-      return (uint32_t)(k4.x >= t_hi) | (uint32_t)(k4.y >= t_hi) << 1 |
-             (uint32_t)(k4.z >= t_hi) << 2 | (uint32_t)(k4.w >= t_hi) << 3;
-    return (uint32_t)selected(k4.x, i) | (uint32_t)selected(k4.y, i + 1) << 1 |
-           (uint32_t)selected(k4.z, i + 2) << 2 | (uint32_t)selected(k4.w, i + 3) << 3;
+  // write selected entry i (with key h) at output position pos (< k)
+  auto emit = [&](int i, uint32_t h, uint32_t pos) {
+    if (MERGE) {
+      sorted[pos] = i;  // the entry; its id is loaded below, all at once
+    } else {
+      // the score from its key (exact; a zero is re-read, the key merges -0 and +0)
+      p.cand_score[li * p.k + pos] = h == 0x80000000u ? src.score(i) : key_score(h);
+      p.cand_idx[li * p.k + pos] = src.gid(i);
+    }
   };
-  if (tid == 0) sh.base = 0u;
-  for (int c0 = 0; c0 < rounds; c0 += kTkBlockRounds) {
-    const int nr = min(kTkBlockRounds, rounds - c0);
-    uint32_t selmask = 0;  // 4 bits per round of the block
-    for (int cr = 0; cr < nr; ++cr) {
-      const int c = c0 + cr;
-      const uint32_t m4 = sel4(get4(c), c * kTkRound + 4 * tid);
-      selmask |= m4 << (4 * cr);
-      const uint32_t wsum = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(m4));
-      if (lane == 0) sh.cw[cr][warp] = wsum;
+  if (staged) {
+    // stable compaction, each thread over a contiguous run of E <= 32 entries (read in a
+    // rotated chunk order: the threads of a warp hit distinct banks): its selection mask,
+    // one block scan of the counts, then its entries written in order
+    const int E = ((n + kTkThreads - 1) / kTkThreads + 3) & ~3;
+    const int nch = E >> 2, lim = rounds * kTkRound;
+    const int e0 = E * tid;
+    uint32_t smask = 0;
+    for (int j = 0; j < nch; ++j) {
+      const int jj = (j + tid) % nch;
+      const int i = e0 + 4 * jj;
+      if (i >= lim) continue;  // (entries past the staged rounds are past the end: key 0)
+      const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
+      uint32_t m4;
+      if (no_ties)
+        m4 = (uint32_t)(k4.x >= t_hi) | (uint32_t)(k4.y >= t_hi) << 1 |
+             (uint32_t)(k4.z >= t_hi) << 2 | (uint32_t)(k4.w >= t_hi) << 3;
+      else
+        m4 = (uint32_t)selected(k4.x, i) | (uint32_t)selected(k4.y, i + 1) << 1 |
+             (uint32_t)selected(k4.z, i + 2) << 2 | (uint32_t)selected(k4.w, i + 3) << 3;
+      smask |= m4 << (4 * jj);
     }
-    __syncthreads();
-    if (warp == 0) {  // exclusive scan of the block's (round, warp) counts in index order
-      const int per = kTkBlockRounds * kTkWarps / 32;
-      uint32_t v[kTkBlockRounds * kTkWarps / 32], run = 0;
-#pragma unroll
-      for (int j = 0; j < per; ++j) {
-        const int q = lane * per + j;
-        v[j] = q / kTkWarps < nr ? sh.cw[q / kTkWarps][q % kTkWarps] : 0u;
-        run += v[j];
-      }
-      uint32_t x = run;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      uint32_t pos = sh.base + x - run;
-#pragma unroll
-      for (int j = 0; j < per; ++j) {
-        const int q = lane * per + j;
-        sh.off[q / kTkWarps][q % kTkWarps] = pos;
-        pos += v[j];
-      }
-      const uint32_t total = __shfl_sync(0xffffffffu, x, 31);
-      __syncwarp();
-      if (lane == 0) sh.base += total;
+    uint32_t total;
+    uint32_t pos = tk_scan((uint32_t)__popc(smask), sh.ws, &total);
+    while (smask != 0u && pos < (uint32_t)p.k) {
+      const int e = __ffs(smask) - 1;
+      smask &= smask - 1u;
+      const int i = e0 + e;
+      emit(i, keys[i], pos++);
     }
+    if (tid == 0) sh.base = total;
     __syncthreads();
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int cr = 0; cr < nr; ++cr) {
-      const int c = c0 + cr;
-      const uint32_t m4 = (selmask >> (4 * cr)) & 15u;
-      // entries of lower lanes come first, then this lane's in order
-      uint32_t pos = sh.off[cr][warp];
+  } else {
+    // lists past the staging: the keys come from L2, in rounds; a block of kTkBlockRounds
+    // rounds at a time: count per (round, warp), one scan, then each warp writes its entries
+    // at positions found with ballots
+    auto sel4 = [&](const uint4& k4, int i) -> uint32_t {  // bit e: entry i + e is selected
+      if (no_ties)
+        return (uint32_t)(k4.x >= t_hi) | (uint32_t)(k4.y >= t_hi) << 1 |
+               (uint32_t)(k4.z >= t_hi) << 2 | (uint32_t)(k4.w >= t_hi) << 3;
+      return (uint32_t)selected(k4.x, i) | (uint32_t)selected(k4.y, i + 1) << 1 |
+             (uint32_t)selected(k4.z, i + 2) << 2 | (uint32_t)selected(k4.w, i + 3) << 3;
+    };
+    if (tid == 0) sh.base = 0u;
+    for (int c0 = 0; c0 < rounds; c0 += kTkBlockRounds) {
+      const int nr = min(kTkBlockRounds, rounds - c0);
+      uint32_t selmask = 0;  // 4 bits per round of the block
+      for (int cr = 0; cr < nr; ++cr) {
+        const int c = c0 + cr;
+        const uint32_t m4 = sel4(get4(c), c * kTkRound + 4 * tid);
+        selmask |= m4 << (4 * cr);
+        const uint32_t wsum = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(m4));
+        if (lane == 0) sh.cw[cr][warp] = wsum;
+      }
+      __syncthreads();
+      if (warp == 0) {  // exclusive scan of the block's (round, warp) counts in index order
+        const int per = kTkBlockRounds * kTkWarps / 32;
+        uint32_t v[kTkBlockRounds * kTkWarps / 32], run = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) pos += __popc(__ballot_sync(0xffffffffu, (m4 >> e) & 1u) & lt);
-      if (m4 == 0u) continue;
-      const int i = c * kTkRound + 4 * tid;
-      uint4 k4 = make_uint4(0u, 0u, 0u, 0u);
-      if (!MERGE) k4 = get4(c);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (((m4 >> e) & 1u) && pos < (uint32_t)p.k) {
-          if (MERGE) {
-            sorted[pos] = i + e;  // the entry; its id is loaded below, all at once
-          } else {
-            // the score from its key (exact; a zero is re-read, the key merges -0 and +0)
-            const uint32_t h = e == 0 ? k4.x : e == 1 ? k4.y : e == 2 ? k4.z : k4.w;
-            p.cand_score[li * p.k + pos] = h == 0x80000000u ? src.score(i + e) : key_score(h);
-            p.cand_idx[li * p.k + pos] = src.gid(i + e);
-          }
+        for (int j = 0; j < per; ++j) {
+          const int q = lane * per + j;
+          v[j] = q / kTkWarps < nr ? sh.cw[q / kTkWarps][q % kTkWarps] : 0u;
+          run += v[j];
         }
-        pos += (m4 >> e) & 1u;
+        uint32_t x = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        uint32_t pos = sh.base + x - run;
+#pragma unroll
+        for (int j = 0; j < per; ++j) {
+          const int q = lane * per + j;
+          sh.off[q / kTkWarps][q % kTkWarps] = pos;
+          pos += v[j];
+        }
+        const uint32_t total = __shfl_sync(0xffffffffu, x, 31);
+        __syncwarp();
+        if (lane == 0) sh.base += total;
       }
+      __syncthreads();
+      const uint32_t lt = (1u << lane) - 1u;
+      for (int cr = 0; cr < nr; ++cr) {
+        const int c = c0 + cr;
+        const uint32_t m4 = (selmask >> (4 * cr)) & 15u;
+        // entries of lower lanes come first, then this lane's in order
+        uint32_t pos = sh.off[cr][warp];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pos += __popc(__ballot_sync(0xffffffffu, (m4 >> e) & 1u) & lt);
+        if (m4 == 0u) continue;
+        const int i = c * kTkRound + 4 * tid;
+        const uint4 k4 = get4(c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (((m4 >> e) & 1u) && pos < (uint32_t)p.k)
+            emit(i + e, e == 0 ? k4.x : e == 1 ? k4.y : e == 2 ? k4.z : k4.w, pos);
+          pos += (m4 >> e) & 1u;
+        }
+      }
+      __syncthreads();  // the offsets are read before the next block rewrites them
     }
-    __syncthreads();  // the offsets are read before the next block rewrites them
   }
   const int cnt = (int)min(sh.base, (uint32_t)p.k);
 
