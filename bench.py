@@ -418,6 +418,9 @@ def main():
     ap.add_argument("--kernel-path", default="auto", choices=["auto", "cuda_cores"],
                     help="decode kernel choice passed to every decode call (cuda_cores: the "
                          "CUDA-core kernel for every head count, for profiling it)")
+    ap.add_argument("--kvwrite-only", action="store_true",
+                    help="time only the DCP KV-cache write (for profiling its kernel) and print "
+                         "its measurement")
     ap.add_argument("--topk-only", action="store_true",
                     help="time only the DSA top-k producer (for profiling its kernels) and "
                          "print its measurement")
@@ -437,6 +440,12 @@ def main():
     dcp.load()
 
     peaks = load_peaks()
+    if args.kvwrite_only:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        res = time_kv_cache_write(dcp, dev, peaks, torch.cuda.current_stream(dev), flush,
+                                  max(3, args.steps))
+        print(json.dumps({"kv_cache_write": res}), flush=True)
+        return
     if args.topk_only:
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         res = time_topk_producer(dcp, dev, peaks, torch.cuda.current_stream(dev), flush,

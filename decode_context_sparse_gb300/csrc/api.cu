@@ -71,6 +71,7 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   p.kv_len = a->kv_len;
   p.D = fused ? dcp : 1;
   p.I = fused ? interleave : 1;
+  p.rule = make_owner_rule(p.D, p.I);
   p.num_units = units;
   p.num_splits = splits;
   p.out = a->out;

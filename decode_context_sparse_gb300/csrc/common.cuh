@@ -17,10 +17,48 @@ constexpr int kTokBytesFP8 = 656;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Owner rule: global slot t -> (shard, local slot).  I = interleave, D = shards.
-__device__ __forceinline__ int owner_of(int t, int D, int I) { return (t / I) % D; }
-__device__ __forceinline__ int local_of(int t, int D, int I) {
-  return (t / (I * D)) * I + (t % I);
+// Exact n / d for 0 <= n < 2^31 and 1 <= d < 2^31 without a division instruction:
+// (n * m) >> s with s = 32 + ceil(log2 d) and m = ceil(2^s / d).  The error term
+// n (m - 2^s / d) / 2^s is below 2^31 / 2^s <= 1 / (2d), so it never carries the quotient
+// past the next integer; n * m < 2^64.
+struct FastDiv {
+  uint64_t m;
+  int s, d;
+};
+__host__ inline FastDiv make_fastdiv(int d) {
+  int l = 0;
+  while ((1ll << l) < (long long)d) ++l;
+  FastDiv f;
+  f.d = d;
+  f.s = 32 + l;
+  f.m = ((1ull << f.s) + (uint64_t)d - 1ull) / (uint64_t)d;
+  return f;
+}
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  return (int)(((uint64_t)(uint32_t)n * f.m) >> f.s);
+}
+
+// Owner rule of D shards with interleave I: global slot t lives on shard (t / I) mod D at
+// local slot (t / (I D)) I + t mod I.  Both from two divisions: q1 = t / I, q2 = t / (I D)
+// = q1 / D, so the shard is q1 - D q2 and t mod I = t - I q1.
+struct OwnerRule {
+  FastDiv I, ID;
+  int D;
+};
+__host__ inline OwnerRule make_owner_rule(int D, int I) {
+  OwnerRule r;
+  r.I = make_fastdiv(I);
+  r.ID = make_fastdiv(I * D);
+  r.D = D;
+  return r;
+}
+__device__ __forceinline__ int owner_of(int t, const OwnerRule& r) {
+  return fdiv(t, r.I) - r.D * fdiv(t, r.ID);
+}
+__device__ __forceinline__ void owner_local(int t, const OwnerRule& r, int& s, int& l) {
+  const int q1 = fdiv(t, r.I), q2 = fdiv(t, r.ID);
+  s = q1 - r.D * q2;
+  l = q2 * r.I.d + (t - q1 * r.I.d);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

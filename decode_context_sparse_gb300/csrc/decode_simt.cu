@@ -36,8 +36,8 @@ __device__ __forceinline__ const uint8_t* resolve_slot(const DecodeParams& p, in
   if (FUSED) {
     const int t = SPARSE ? __ldg(idx_row + pos) : pos;
     if (t < 0) return nullptr;
-    const int s = owner_of(t, p.D, p.I);
-    l = local_of(t, p.D, p.I);
+    int s;
+    owner_local(t, p.rule, s, l);
     table = p.bt + (int64_t)s * p.num_seqs * p.bt_stride;
   } else {
     l = SPARSE ? __ldg(idx_row + pos) : pos;

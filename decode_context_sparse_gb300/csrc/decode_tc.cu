@@ -445,8 +445,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         int l;
         const int32_t* table;
         if (FUSED) {
-          const int s = owner_of(t_v, p.D, p.I);
-          l = local_of(t_v, p.D, p.I);
+          int s;
+          owner_local(t_v, p.rule, s, l);
           table = p.bt + ((int64_t)s * p.num_seqs + t_x.b) * p.bt_stride;
         } else {
           l = t_v;

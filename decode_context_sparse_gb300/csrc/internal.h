@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/dcpmla.h"
+#include "common.cuh"
 
 namespace dcp {
 
@@ -27,6 +28,7 @@ struct DecodeParams {
   int k;
   const int32_t* kv_len;  // dense lengths (local for partial, global for fused)
   int D, I;               // fused: owner rule
+  OwnerRule rule;         // the same as fast divisions
   int64_t num_units;      // partial: shards * rows; fused: rows
   int num_splits;
   void* out;              // partial: fp32 [units][H][512]; fused: bf16 [rows][H][512]

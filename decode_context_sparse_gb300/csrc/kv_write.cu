@@ -13,10 +13,11 @@
 // resolved, so the three loads overlap.
 //
 // The quotients.  q = v * r with r the correctly rounded 1/scale lies within 2 ulps of the
-// correctly rounded v / scale (two roundings of relative size 2^-24 each).  E4M3 rounding is
-// monotone, so when q - 3 ulps and q + 3 ulps convert to the same code as q, so does the
-// exact quotient; otherwise (q near an E4M3 rounding boundary, about one value in 10^5) that
-// pair is divided exactly.  The codes are those of the IEEE quotients in every case.
+// correctly rounded v / scale (two roundings of relative size 2^-24 each).  E4M3 rounding
+// changes only at the midpoints between neighbouring E4M3 values, so when q is more than 3
+// ulps from every midpoint (an integer test on its bits) the exact quotient has the same
+// code; otherwise (about one value in 10^5, or a value below E4M3's normal range) that pair
+// is divided exactly.  The codes are those of the IEEE quotients in every case.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,27 +33,27 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// q moved by d units in the last place, away from (d > 0) or towards (d < 0) zero; values
-// within 3 ulps of zero stay put (they are far below the smallest E4M3 step)
-__device__ __forceinline__ float ulp_nudge(float q, int d) {
-  const uint32_t u = __float_as_uint(q);
-  return (u & 0x7fffffffu) < 4u ? q : __uint_as_float(u + d);
+// True when the E4M3 rounding of a quotient within 2 ulps of q might differ from that of q:
+// q lies within 3 ulps of a rounding midpoint of E4M3, or below E4M3's normal range.  For
+// 2^-6 <= |q|, an E4M3 step is 2^20 fp32 ulps and the midpoints are the values whose low 20
+// mantissa bits are 0x80000 (also at the top of a binade); above 448 every value saturates
+// to 448.  Below 2^-6 (subnormal E4M3) the quotient is always computed exactly.
+__device__ __forceinline__ bool e4m3_near_midpoint(float q) {
+  const uint32_t u = __float_as_uint(q) & 0x7fffffffu;
+  return u < 0x3c800000u || ((u & 0xfffffu) - 0x7fffdu) < 7u;
 }
 
 // The E4M3 codes of a / s and b / s (IEEE quotients), from products with r = 1 / s.
 __device__ __forceinline__ uint32_t e4m3x2_of_quotients(float a, float b, float s, float r) {
   const float qa = a * r, qb = b * r;
-  const uint32_t c = f32x2_to_e4m3x2(qa, qb);
-  const uint32_t cl = f32x2_to_e4m3x2(ulp_nudge(qa, -3), ulp_nudge(qb, -3));
-  const uint32_t ch = f32x2_to_e4m3x2(ulp_nudge(qa, 3), ulp_nudge(qb, 3));
-  if (c == cl && c == ch) return c;
-  return f32x2_to_e4m3x2(a / s, b / s);
+  if (e4m3_near_midpoint(qa) || e4m3_near_midpoint(qb)) return f32x2_to_e4m3x2(a / s, b / s);
+  return f32x2_to_e4m3x2(qa, qb);
 }
 
 template <int KVT>
 __global__ void __launch_bounds__(kKvwThreads)
 kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restrict__ seq,
-                const int32_t* __restrict__ pos, int D, int I, int shard, uint8_t* pool,
+                const int32_t* __restrict__ pos, const OwnerRule rule, int shard, uint8_t* pool,
                 int64_t num_pages, const int32_t* __restrict__ bt, int num_seqs, int bt_stride,
                 int32_t* err) {
   const int lane = threadIdx.x & 31;
@@ -83,9 +84,9 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
       if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
       continue;
     }
-    const int s = owner_of(t, D, I);
+    int s, l;
+    owner_local(t, rule, s, l);
     if (shard >= 0 && s != shard) continue;
-    const int l = local_of(t, D, I);
     const int pj = l >> 6;  // page size 64
     if (pj >= bt_stride) {
       if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
@@ -139,12 +140,13 @@ cudaError_t launch_kv_write(const void* kv, int64_t n, const int32_t* seq, const
   const int grid = (int)(need < (int64_t)sms * 16 ? need : (int64_t)sms * 16);
   const uint4* k4 = static_cast<const uint4*>(kv);
   uint8_t* p8 = static_cast<uint8_t*>(pool);
+  const OwnerRule rule = make_owner_rule(D, I);
   if (kv_dtype == DCP_KV_BF16)
-    kv_write_kernel<DCP_KV_BF16><<<grid, kKvwThreads, 0, st>>>(k4, n, seq, pos, D, I, shard, p8,
+    kv_write_kernel<DCP_KV_BF16><<<grid, kKvwThreads, 0, st>>>(k4, n, seq, pos, rule, shard, p8,
                                                                num_pages, bt, num_seqs, bt_stride, err);
   else
     kv_write_kernel<DCP_KV_FP8_E4M3_S128><<<grid, kKvwThreads, 0, st>>>(
-        k4, n, seq, pos, D, I, shard, p8, num_pages, bt, num_seqs, bt_stride, err);
+        k4, n, seq, pos, rule, shard, p8, num_pages, bt, num_seqs, bt_stride, err);
   return cudaGetLastError();
 }
 

@@ -19,8 +19,9 @@ namespace dcp {
 constexpr int kRemapWarps = 8;
 
 __global__ void __launch_bounds__(kRemapWarps * 32)
-remap_topk_kernel(const int32_t* __restrict__ gidx, int k, int D, int I, int shard,
+remap_topk_kernel(const int32_t* __restrict__ gidx, int k, const OwnerRule rule, int shard,
                   int32_t* __restrict__ local_idx, int32_t* __restrict__ count, int64_t rows) {
+  const int D = rule.D;
   __shared__ int cnt[kRemapWarps][DCP_MAX_SHARDS];
   __shared__ int base[kRemapWarps][DCP_MAX_SHARDS];
   __shared__ int total[DCP_MAX_SHARDS];
@@ -44,7 +45,7 @@ remap_topk_kernel(const int32_t* __restrict__ gidx, int k, int D, int I, int sha
     if (pos < p1) {
       const int t = __ldg(g + pos);
       if (t >= 0) {
-        const int s = owner_of(t, D, I);
+        const int s = owner_of(t, rule);
         if (s - s0 >= 0 && s - s0 < n_out) key = s - s0;
       }
     }
@@ -74,10 +75,11 @@ remap_topk_kernel(const int32_t* __restrict__ gidx, int k, int D, int I, int sha
     if (pos < p1) {
       const int t = __ldg(g + pos);
       if (t >= 0) {
-        const int s = owner_of(t, D, I);
+        int s, l;
+        owner_local(t, rule, s, l);
         if (s - s0 >= 0 && s - s0 < n_out) {
           key = s - s0;
-          loc = local_of(t, D, I);
+          loc = l;
         }
       }
     }
@@ -114,8 +116,8 @@ __global__ void local_lengths_kernel(const int32_t* __restrict__ glen, int64_t r
 cudaError_t launch_remap_topk(const int32_t* gidx, int64_t rows, int k, int D, int I, int shard,
                               int32_t* local_idx, int32_t* count, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
-  remap_topk_kernel<<<(unsigned)rows, kRemapWarps * 32, 0, st>>>(gidx, k, D, I, shard, local_idx,
-                                                                 count, rows);
+  remap_topk_kernel<<<(unsigned)rows, kRemapWarps * 32, 0, st>>>(
+      gidx, k, make_owner_rule(D, I), shard, local_idx, count, rows);
   return cudaGetLastError();
 }
 

@@ -261,3 +261,18 @@ def test_cfg3_full_size_all_rows(dcp):
 
 def test_cfg5_full_size_all_rows(dcp):
     _full_size(dcp, synth.cfg5_dense_long(device=DEV))
+
+
+@pytest.mark.parametrize("D,I", [(3, 1), (7, 5), (63, 1), (5, 1000), (64, 64), (2, 65536)])
+def test_remap_large_ids_odd_rules(dcp, D, I):
+    """Global slot ids up to 2^31 - 1 and divisors that are not powers of two: the owner rule
+    (shard and local slot) must be bit-exact against the oracle everywhere in the id range."""
+    g = torch.Generator().manual_seed(D * 1009 + I)
+    rows, k = 19, 3000
+    ids = torch.randint(0, 2**31 - 1, (rows, k), generator=g, dtype=torch.int64)
+    ids[0, :8] = torch.tensor([0, 1, I - 1, I, I * D - 1, I * D, 2**31 - 2, 2**31 - 1])
+    ids[1] = torch.arange(k, dtype=torch.int64) * 977 + (2**31 - 1 - 977 * k)
+    ids = ids.to(torch.int32)
+    loc, cnt = dcp.dcp_remap_topk(ids.to(DEV), D, I)
+    rloc, rcnt = oracle.remap(ids, D, I)
+    assert np.array_equal(cnt.cpu().numpy(), rcnt) and np.array_equal(loc.cpu().numpy(), rloc)
