@@ -12,12 +12,14 @@
 // written per row.  A row's data is loaded before its position and block-table entry are
 // resolved, so the three loads overlap.
 //
-// The quotients.  q = v * r with r the correctly rounded 1/scale lies within 2 ulps of the
-// correctly rounded v / scale (two roundings of relative size 2^-24 each).  E4M3 rounding
-// changes only at the midpoints between neighbouring E4M3 values, so when q is more than 3
-// ulps from every midpoint (an integer test on its bits) the exact quotient has the same
-// code; otherwise (about one value in 10^5, or a value below E4M3's normal range) that pair
-// is divided exactly.  The codes are those of the IEEE quotients in every case.
+// The quotients.  With r = 1 / scale correctly rounded, q0 = v * r lies within one ulp of
+// v / scale; the residual e = q0 * scale - v is exact in one fused multiply-add, and
+// q = q0 - e * r (one more fused multiply-add) is the correctly rounded quotient v / scale
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990: the correction step with a correctly rounded
+// reciprocal).  The theorem needs normal operands: a block whose scale lies outside
+// [2^-100, FLT_MAX] takes IEEE divisions instead.  So the codes are those of the IEEE
+// quotients, with three floating-point operations per value and no branch.
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,21 +35,21 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return r;
 }
 
-// True when the E4M3 rounding of a quotient within 2 ulps of q might differ from that of q:
-// q lies within 3 ulps of a rounding midpoint of E4M3, or below E4M3's normal range.  For
-// 2^-6 <= |q|, an E4M3 step is 2^20 fp32 ulps and the midpoints are the values whose low 20
-// mantissa bits are 0x80000 (also at the top of a binade); above 448 every value saturates
-// to 448.  Below 2^-6 (subnormal E4M3) the quotient is always computed exactly.
-__device__ __forceinline__ bool e4m3_near_midpoint(float q) {
-  const uint32_t u = __float_as_uint(q) & 0x7fffffffu;
-  return u < 0x3c800000u || ((u & 0xfffffu) - 0x7fffdu) < 7u;
+// Largest of two bf16 pairs, lane by lane; a NaN never wins over a number (max.bf16x2
+// returns the non-NaN operand), as with a float comparison.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
-// The E4M3 codes of a / s and b / s (IEEE quotients), from products with r = 1 / s.
-__device__ __forceinline__ uint32_t e4m3x2_of_quotients(float a, float b, float s, float r) {
-  const float qa = a * r, qb = b * r;
-  if (e4m3_near_midpoint(qa) || e4m3_near_midpoint(qb)) return f32x2_to_e4m3x2(a / s, b / s);
-  return f32x2_to_e4m3x2(qa, qb);
+// v / scale correctly rounded, from r = 1 / scale correctly rounded (Markstein correction).
+// The residual is taken as q0 * scale - v and subtracted, so that v = -0 gives -0, as the
+// IEEE quotient does (the sign of a zero decides its E4M3 code).
+__device__ __forceinline__ float quotient_rn(float v, float scale, float r) {
+  const float q0 = v * r;
+  const float e = fmaf(q0, scale, -v);
+  return fmaf(-e, r, q0);
 }
 
 template <int KVT>
@@ -105,25 +107,34 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
     } else {
       uint8_t* row = pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesFP8;
       const uint32_t w[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-      float v[16];
-      float amax = 0.f;
+      // the block's largest magnitude: packed bf16 maxima of the magnitudes
+      uint32_t mx = 0u;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        v[2 * e] = bf16_lo(w[e]);
-        v[2 * e + 1] = bf16_hi(w[e]);
-        amax = fmaxf(amax, fmaxf(fabsf(v[2 * e]), fabsf(v[2 * e + 1])));
-      }
+      for (int e = 0; e < 8; ++e) mx = bf16x2_max(mx, w[e] & 0x7fff7fffu);
 #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      for (int o = 1; o < 8; o <<= 1) mx = bf16x2_max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float amax = fmaxf(bf16_lo(mx), bf16_hi(mx));
       const float scale = amax / 448.0f;
-      uint32_t q[4] = {0u, 0u, 0u, 0u};
-      if (scale > 0.f) {
+      float qv[16];
+      if (scale >= 0x1p-100f && scale <= 3.40282347e38f) {
         const float r = 1.0f / scale;  // correctly rounded
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          q[e] = e4m3x2_of_quotients(v[4 * e], v[4 * e + 1], scale, r) |
-                 (e4m3x2_of_quotients(v[4 * e + 2], v[4 * e + 3], scale, r) << 16);
+        for (int e = 0; e < 8; ++e) {
+          qv[2 * e] = quotient_rn(bf16_lo(w[e]), scale, r);
+          qv[2 * e + 1] = quotient_rn(bf16_hi(w[e]), scale, r);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          qv[2 * e] = scale > 0.f ? bf16_lo(w[e]) / scale : 0.f;
+          qv[2 * e + 1] = scale > 0.f ? bf16_hi(w[e]) / scale : 0.f;
+        }
       }
+      uint32_t q[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        q[e] = f32x2_to_e4m3x2(qv[4 * e], qv[4 * e + 1]) |
+               (f32x2_to_e4m3x2(qv[4 * e + 2], qv[4 * e + 3]) << 16);
       *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
       if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + 4 * (lane >> 3)) = scale;
       if (lane < 8) *reinterpret_cast<uint4*>(row + 528 + 16 * lane) = d2;

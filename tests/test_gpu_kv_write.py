@@ -192,3 +192,41 @@ def test_kv_write_quotients_near_e4m3_boundaries(dcp, orc):
     dcp.dcp_kv_cache_write(kv.cuda(), seq.cuda(), pos.cuda(), d_pool, synth.KV_FP8, bt.cuda(), 1, 1)
     torch.cuda.synchronize()
     assert np.array_equal(d_pool.cpu().numpy(), ref)
+
+
+def test_kv_write_signed_zeros_and_extreme_scales(dcp, orc):
+    """Blocks the quotient method treats with care: -0 and +0 beside nonzero values (the sign
+    of a zero decides its code), bf16 subnormals, a block of zeros of both signs (scale 0),
+    blocks whose scale lies below 2^-100 or near the top of the fp32 range (exact divisions),
+    and quotients just around the smallest E4M3 subnormal's rounding midpoint."""
+    gen = torch.Generator().manual_seed(21)
+    rows = []
+    base = torch.randn((8, 576), generator=gen)
+    r = base.clone()
+    r[0, 1:64:2] = -0.0
+    r[0, 2:64:2] = 0.0
+    r[1, 0:128] = torch.randn(128, generator=gen) * 2.0 ** -128   # bf16 subnormals
+    r[1, 128:256] = 0.0
+    r[1, 128:256:3] = -0.0                                      # all-zero block, both signs
+    r[2, 0:128] = torch.randn(128, generator=gen) * 2.0 ** -95  # scale below 2^-100
+    r[2, 128:256] = torch.randn(128, generator=gen) * 2.0 ** 126  # scale near 2^118
+    r[3, 0] = 448.0                                             # scale exactly 1
+    r[3, 1:128] = torch.linspace(2.0 ** -11, 2.0 ** -9, 127)      # around 2^-10, the midpoint
+    r[3, 128] = -448.0
+    r[3, 129:256] = -torch.linspace(2.0 ** -11, 2.0 ** -9, 127)
+    rows.append(r)
+    kv = torch.cat(rows).to(torch.bfloat16)
+    assert bool(torch.signbit(kv[0, 1])) and kv[0, 1] == 0
+    n = kv.shape[0]
+    seq = torch.zeros(n, dtype=torch.int32)
+    pos = torch.arange(n, dtype=torch.int32)
+    bt = torch.arange(1, dtype=torch.int32).view(1, 1, 1)
+    pool = torch.zeros((1, P, 656), dtype=torch.uint8)
+    ref, written, _ = orc.kv_write(kv, seq, pos, pool, synth.KV_FP8, bt, 1, 1)
+    assert written == n
+    d_pool = pool.cuda()
+    dcp.dcp_kv_cache_write(kv.cuda(), seq.cuda(), pos.cuda(), d_pool, synth.KV_FP8, bt.cuda(), 1, 1)
+    torch.cuda.synchronize()
+    got = d_pool.cpu().numpy()
+    assert (ref[0, 0, 1:64:2] == 0x80).all() and (ref[0, 0, 2:64:2] == 0x00).all()
+    assert np.array_equal(got, ref)
