@@ -52,6 +52,91 @@ __device__ __forceinline__ float quotient_rn(float v, float scale, float r) {
   return fmaf(-e, r, q0);
 }
 
+// This warp's share of one token row: 16 B loads at the offsets the writer uses.
+template <int KVT>
+__device__ __forceinline__ void load_row(const uint4* __restrict__ kv, int64_t i, int lane,
+                                         uint4& d0, uint4& d1, uint4& d2) {
+  const uint4* src = kv + i * (kDqk * 2 / 16);  // 72 chunks of 16 B
+  d2 = make_uint4(0u, 0u, 0u, 0u);
+  if (KVT == DCP_KV_BF16) {
+    d0 = __ldg(src + lane);
+    d1 = __ldg(src + 32 + lane);
+  } else {
+    d0 = __ldg(src + 2 * lane);
+    d1 = __ldg(src + 2 * lane + 1);
+  }
+  if (lane < 8) d2 = __ldg(src + 64 + lane);  // RoPE (BF16: the row's last 128 B)
+}
+
+// Resolve where token t of sequence b goes and write it there (FP8: quantised).
+template <int KVT>
+__device__ __forceinline__ void write_row(const uint4& d0, const uint4& d1, const uint4& d2,
+                                          int t, int b, int lane, const OwnerRule& rule,
+                                          int shard, uint8_t* pool, int64_t num_pages,
+                                          const int32_t* __restrict__ bt, int num_seqs,
+                                          int bt_stride, int32_t* err) {
+  if (t < 0) return;  // padding
+  if (b < 0 || b >= num_seqs) {
+    if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
+    return;
+  }
+  int s, l;
+  owner_local(t, rule, s, l);
+  if (shard >= 0 && s != shard) return;
+  const int pj = l >> 6;  // page size 64
+  if (pj >= bt_stride) {
+    if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
+    return;
+  }
+  const int page = __ldg(bt + ((int64_t)s * num_seqs + b) * bt_stride + pj);
+  if (page < 0 || page >= num_pages) {
+    if (lane == 0) set_err(err, DCP_ERRBIT_PAGE_RANGE);
+    return;
+  }
+  if (KVT == DCP_KV_BF16) {
+    uint4* dst = reinterpret_cast<uint4*>(pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesBF16);
+    dst[lane] = d0;
+    dst[32 + lane] = d1;
+    if (lane < 8) dst[64 + lane] = d2;
+    return;
+  }
+  const uint32_t w[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+  uint8_t* row = pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesFP8;
+  // the block's largest magnitude: packed bf16 maxima of the magnitudes
+  uint32_t mx = 0u;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mx = bf16x2_max(mx, w[e] & 0x7fff7fffu);
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) mx = bf16x2_max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float amax = fmaxf(bf16_lo(mx), bf16_hi(mx));
+  const float scale = amax / 448.0f;
+  float qv[16];
+  if (scale >= 0x1p-100f && scale <= 3.40282347e38f) {
+    const float r = 1.0f / scale;  // correctly rounded
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      qv[2 * e] = quotient_rn(bf16_lo(w[e]), scale, r);
+      qv[2 * e + 1] = quotient_rn(bf16_hi(w[e]), scale, r);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      qv[2 * e] = scale > 0.f ? bf16_lo(w[e]) / scale : 0.f;
+      qv[2 * e + 1] = scale > 0.f ? bf16_hi(w[e]) / scale : 0.f;
+    }
+  }
+  uint32_t q[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    q[e] = f32x2_to_e4m3x2(qv[4 * e], qv[4 * e + 1]) |
+           (f32x2_to_e4m3x2(qv[4 * e + 2], qv[4 * e + 3]) << 16);
+  *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
+  if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + 4 * (lane >> 3)) = scale;
+  if (lane < 8) *reinterpret_cast<uint4*>(row + 528 + 16 * lane) = d2;
+}
+
+// A warp's rows are i0, i0 + stride, ...; the next row's data, position and sequence are
+// loaded before the current row is resolved and written, so two rows' loads are in flight.
 template <int KVT>
 __global__ void __launch_bounds__(kKvwThreads)
 kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restrict__ seq,
@@ -61,84 +146,26 @@ kv_write_kernel(const uint4* __restrict__ kv, int64_t n, const int32_t* __restri
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kKvwRowsPerCta;
   const int64_t i0 = (int64_t)blockIdx.x * kKvwRowsPerCta + (threadIdx.x >> 5);
-  // position and sequence of this warp's next row, loaded one row ahead
-  int t_next = i0 < n ? __ldg(pos + i0) : -1, b_next = i0 < n ? __ldg(seq + i0) : -1;
+  if (i0 >= n) return;
+  uint4 d0, d1, d2;
+  load_row<KVT>(kv, i0, lane, d0, d1, d2);
+  int t = __ldg(pos + i0), b = __ldg(seq + i0);
   for (int64_t i = i0; i < n; i += stride) {
-    // the row's data first: its loads overlap the position / block-table chain below
-    const uint4* src = kv + i * (kDqk * 2 / 16);  // 72 chunks of 16 B
-    uint4 d0, d1, d2 = make_uint4(0u, 0u, 0u, 0u);
-    if (KVT == DCP_KV_BF16) {
-      d0 = __ldg(src + lane);
-      d1 = __ldg(src + 32 + lane);
-      if (lane < 8) d2 = __ldg(src + 64 + lane);
-    } else {
-      d0 = __ldg(src + 2 * lane);
-      d1 = __ldg(src + 2 * lane + 1);
-      if (lane < 8) d2 = __ldg(src + 64 + lane);  // RoPE
+    const int64_t j = i + stride;
+    uint4 e0 = d0, e1 = d1, e2 = d2;
+    int tn = -1, bn = -1;
+    if (j < n) {
+      load_row<KVT>(kv, j, lane, e0, e1, e2);
+      tn = __ldg(pos + j);
+      bn = __ldg(seq + j);
     }
-    const int t = t_next, b = b_next;
-    if (i + stride < n) {
-      t_next = __ldg(pos + i + stride);
-      b_next = __ldg(seq + i + stride);
-    }
-    if (t < 0) continue;  // padding
-    if (b < 0 || b >= num_seqs) {
-      if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
-      continue;
-    }
-    int s, l;
-    owner_local(t, rule, s, l);
-    if (shard >= 0 && s != shard) continue;
-    const int pj = l >> 6;  // page size 64
-    if (pj >= bt_stride) {
-      if (lane == 0) set_err(err, DCP_ERRBIT_SLOT_RANGE);
-      continue;
-    }
-    const int page = __ldg(bt + ((int64_t)s * num_seqs + b) * bt_stride + pj);
-    if (page < 0 || page >= num_pages) {
-      if (lane == 0) set_err(err, DCP_ERRBIT_PAGE_RANGE);
-      continue;
-    }
-    if (KVT == DCP_KV_BF16) {
-      uint4* dst = reinterpret_cast<uint4*>(pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesBF16);
-      dst[lane] = d0;
-      dst[32 + lane] = d1;
-      if (lane < 8) dst[64 + lane] = d2;
-    } else {
-      uint8_t* row = pool + ((int64_t)page * 64 + (l & 63)) * kTokBytesFP8;
-      const uint32_t w[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-      // the block's largest magnitude: packed bf16 maxima of the magnitudes
-      uint32_t mx = 0u;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx = bf16x2_max(mx, w[e] & 0x7fff7fffu);
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) mx = bf16x2_max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float amax = fmaxf(bf16_lo(mx), bf16_hi(mx));
-      const float scale = amax / 448.0f;
-      float qv[16];
-      if (scale >= 0x1p-100f && scale <= 3.40282347e38f) {
-        const float r = 1.0f / scale;  // correctly rounded
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          qv[2 * e] = quotient_rn(bf16_lo(w[e]), scale, r);
-          qv[2 * e + 1] = quotient_rn(bf16_hi(w[e]), scale, r);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          qv[2 * e] = scale > 0.f ? bf16_lo(w[e]) / scale : 0.f;
-          qv[2 * e + 1] = scale > 0.f ? bf16_hi(w[e]) / scale : 0.f;
-        }
-      }
-      uint32_t q[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        q[e] = f32x2_to_e4m3x2(qv[4 * e], qv[4 * e + 1]) |
-               (f32x2_to_e4m3x2(qv[4 * e + 2], qv[4 * e + 3]) << 16);
-      *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(q[0], q[1], q[2], q[3]);
-      if ((lane & 7) == 0) *reinterpret_cast<float*>(row + 512 + 4 * (lane >> 3)) = scale;
-      if (lane < 8) *reinterpret_cast<uint4*>(row + 528 + 16 * lane) = d2;
-    }
+    write_row<KVT>(d0, d1, d2, t, b, lane, rule, shard, pool, num_pages, bt, num_seqs,
+                   bt_stride, err);
+    d0 = e0;
+    d1 = e1;
+    d2 = e2;
+    t = tn;
+    b = bn;
   }
 }
 

@@ -8,15 +8,17 @@
 // k best of its n entries by radix selection on a 64-bit key.  The high word is an
 // order-preserving image of the fp32 score (NaN, -inf and padding ids map to 0 and are never
 // selected; -0 maps like +0); the low word is the complement of the global slot id, so a
-// larger key ranks first and the keys of one list are distinct.  Digits of 11, 11 and 10
-// bits of each word are resolved from the top: a digit's histogram (shared-memory atomics)
-// locates the bin of the k-th largest key among those still in play, and the search stops
-// as soon as that bin is taken whole (two digits for continuous scores).  The high words of
-// a list of up to kTkStageMax entries are staged in shared memory while the first digit's
-// histogram is built from the global loads; longer lists re-read global memory (L2) for
-// each further digit.  The selection is written in increasing slot order: a candidate list
-// by a stable compaction (local slot order is global slot order on a shard), the merge by a
-// bitonic sort of the selected ids in shared memory.
+// larger key ranks first and the keys of one list are distinct.  The first digit (the
+// top 11 bits) is resolved by a histogram (shared-memory atomics) built while a list of up
+// to kTkStageMax entries is loaded and staged in shared memory; the bin that holds the k-th
+// largest key then usually holds a few hundred staged entries, whose 16-bit indices become
+// the candidates, and the remaining digits (10 bits each) look at the candidates only.  The
+// search stops as soon as a digit's bin is taken whole.  Lists longer than the staging, or
+// with more candidates than the buffer holds, resolve the further digits (11, 10, then the
+// low word) over every entry, re-reading global memory (L2) when not staged.  The
+// selection is written in increasing slot order: a candidate list by a stable compaction
+// (local slot order is global slot order on a shard), the merge by merging the shards'
+// ascending runs (a bitonic sort when some run is out of order).
 // Comparisons and integer work only: the result is bit-identical to the definition.
 #include <limits.h>
 
@@ -28,18 +30,24 @@ namespace dcp {
 constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkBins = 2048;
+// candidates (the staged entries in the first digit's bin): their histogram takes the first
+// kTkCandBins words of the first digit's, their 16-bit staging indices the rest
+constexpr int kTkCandBins = 1024;
+constexpr int kTkCandCap = (kTkBins - kTkCandBins) * 2;
 constexpr int kTkRound = 4 * kTkThreads;  // entries per round: four consecutive per thread
 constexpr int kTkLoadRounds = 4;          // rounds whose loads are issued together
 constexpr int kTkBlockRounds = kTkStageMax / kTkRound;  // rounds per compaction block
 static_assert(kTkStageMax % kTkRound == 0, "staging holds whole rounds");
+static_assert(kTkStageMax / kTkRound <= 8 && kTkStageMax <= 65536,
+              "a thread's staged entries fit one 32-bit mask; staging indices fit 16 bits");
 
 // Order-preserving image of an fp32 score; 0 for the entries that are never selected.
+// Adding +0 turns -0 into +0 (so that it ranks as +0) and leaves every other value as it is.
+// The image of -inf is 0x007fffff and that of +inf 0xff800000; NaNs map outside that range.
 __device__ __forceinline__ uint32_t score_key(float s) {
-  uint32_t u = __float_as_uint(s);
-  const bool valid = s == s && u != 0xff800000u;  // not NaN, not -inf
-  u = u == 0x80000000u ? 0u : u;                   // -0 ranks as +0
-  const uint32_t flip = (u & 0x80000000u) ? 0xffffffffu : 0x80000000u;
-  return valid ? (u ^ flip) : 0u;
+  const uint32_t u = __float_as_uint(__fadd_rn(s, 0.0f));
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return k - 0x00800000u <= 0xff800000u - 0x00800000u ? k : 0u;
 }
 
 // The fp32 score of a key (inverse of score_key for keys other than 0).
@@ -134,15 +142,17 @@ __device__ __forceinline__ uint32_t tk_scan(uint32_t v, uint32_t* ws, uint32_t* 
   }
   if (lane == 31) ws[warp] = x;
   __syncthreads();
-  uint32_t before = 0, tot = 0;
+  // every warp scans the warp totals itself
+  const uint32_t wt = lane < kTkWarps ? ws[lane] : 0u;
+  uint32_t wx = wt;
 #pragma unroll
-  for (int w = 0; w < kTkWarps; ++w) {
-    const uint32_t t = ws[w];
-    if (w < warp) before += t;
-    tot += t;
+  for (int o = 1; o < kTkWarps; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, wx, o);
+    if (lane >= o) wx += y;
   }
+  const uint32_t before = __shfl_sync(0xffffffffu, wx - wt, warp);
+  *total = __shfl_sync(0xffffffffu, wx, kTkWarps - 1);
   __syncthreads();
-  *total = tot;
   return before + x - v;
 }
 
@@ -150,39 +160,42 @@ struct TkShared {
   uint32_t ws[kTkWarps];
   uint32_t cw[kTkBlockRounds][kTkWarps];   // selected entries per (round, warp) of a block
   uint32_t off[kTkBlockRounds][kTkWarps];  // their output offsets
-  uint32_t bin, above, base;
+  uint32_t bin, above, binh, base;  // a digit's bin, the keys in play above it, its count
   int run[DCP_MAX_SHARDS + 1];  // merge: first selected entry of each shard's list
 };
 
-// The bin (of nb) holding the krem-th largest in-play key, counting from the top bin, and
-// the number of in-play keys in the bins above it.
-__device__ __forceinline__ uint32_t tk_find_bin(const uint32_t* hist, int nb, uint32_t krem,
-                                                TkShared& sh) {
-  const int bpt = nb / kTkThreads;  // bins per thread, taken from the top
-  const int top = nb - 1 - threadIdx.x * bpt;
-  if (threadIdx.x == 0) {  // (a bin is always found: krem never exceeds the keys in play)
-    sh.bin = 0u;
-    sh.above = 0u;
+// The bin (of BPT * kTkThreads) holding the krem-th largest in-play key, counting from the
+// top bin, the number of in-play keys in the bins above it and in the bin (sh.bin,
+// sh.above, sh.binh).  Returns the histogram's total.
+template <int BPT>
+__device__ __forceinline__ uint32_t tk_find_bin(const uint32_t* hist, uint32_t krem, TkShared& sh) {
+  const int top = kTkThreads * BPT - 1 - threadIdx.x * BPT;  // bins top, top - 1, ...
+  uint32_t h[BPT], mine = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    h[j] = hist[top - j];
+    mine += h[j];
   }
-  uint32_t mine = 0;
-  for (int j = 0; j < bpt; ++j) mine += hist[top - j];
   uint32_t tot;
   uint32_t cum = tk_scan(mine, sh.ws, &tot);
-  for (int j = 0; j < bpt; ++j) {
-    const uint32_t h = hist[top - j];
-    if (cum < krem && cum + h >= krem) {
+  // (a bin is always found: krem never exceeds the keys in play)
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    if (cum < krem && cum + h[j] >= krem) {
       sh.bin = (uint32_t)(top - j);
       sh.above = cum;
+      sh.binh = h[j];
     }
-    cum += h;
+    cum += h[j];
   }
   __syncthreads();
-  return tot;  // keys in play
+  return tot;
 }
 
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t h, uint32_t msk, uint32_t pre,
                                          int shift, int nb) {
-  if (h != 0u && (h & msk) == pre) atomicAdd(&hist[(h >> shift) & (nb - 1)], 1u);
+  // (msk covers the first digit and pre's first digit is a bin >= 1: h == 0 never counts)
+  if ((h & msk) == pre) atomicAdd(&hist[(h >> shift) & (nb - 1)], 1u);
 }
 
 template <bool MERGE>
@@ -190,7 +203,11 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint32_t tk_smem[];
   uint32_t* hist = tk_smem;
   uint32_t* keys = tk_smem + kTkBins;                          // p.stage entries
-  int32_t* sorted = reinterpret_cast<int32_t*>(keys + p.stage);  // merge: p.kp entries
+  // merge: two run buffers of p.kp entries; for kp <= kTkBins the histogram's words and the
+  // staging, both free once the selection is compacted, else words past the staging
+  const bool runs_inside = p.kp <= kTkBins;
+  int32_t* sorted = reinterpret_cast<int32_t*>(runs_inside ? hist : keys + p.stage);
+  int32_t* sorted2 = runs_inside ? reinterpret_cast<int32_t*>(keys) : sorted + p.kp;
   __shared__ TkShared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t li = blockIdx.x;
@@ -220,7 +237,8 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
     return staged ? *reinterpret_cast<const uint4*>(keys + i) : src.key4(i);
   };
 
-  // pass 0: stage the keys, count the valid entries, histogram of the first digit
+  // pass 0: stage the keys and build the histogram of the first digit.  Every entry counts,
+  // the invalid ones (key 0, and the entries past the end) in bin 0, which holds no valid key.
   for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
   __syncthreads();
   for (int c0 = 0; c0 < rounds; c0 += kTkLoadRounds) {
@@ -238,72 +256,130 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
     }
 #pragma unroll
     for (int u = 0; u < kTkLoadRounds; ++u) {
-      // (entries of rounds past the end were loaded as -inf: key 0, nothing counted)
-      const uint4 k4 = src.keys_of(v[u], t[u]);
-      if (staged && c0 + u < rounds)  // the staging is a whole number of rounds
-        *reinterpret_cast<uint4*>(keys + (c0 + u) * kTkRound + 4 * tid) = k4;
-      hist_add(hist, k4.x, 0u, 0u, 21, kTkBins);
-      hist_add(hist, k4.y, 0u, 0u, 21, kTkBins);
-      hist_add(hist, k4.z, 0u, 0u, 21, kTkBins);
-      hist_add(hist, k4.w, 0u, 0u, 21, kTkBins);
+      if (c0 + u < rounds) {
+        const uint4 k4 = src.keys_of(v[u], t[u]);
+        if (staged)  // the staging is a whole number of rounds
+          *reinterpret_cast<uint4*>(keys + (c0 + u) * kTkRound + 4 * tid) = k4;
+        atomicAdd(&hist[k4.x >> 21], 1u);
+        atomicAdd(&hist[k4.y >> 21], 1u);
+        atomicAdd(&hist[k4.z >> 21], 1u);
+        atomicAdd(&hist[k4.w >> 21], 1u);
+      }
     }
   }
   __syncthreads();
-  // the first digit's bin; the histogram's total is the number of valid entries
-  const uint32_t nvalid = tk_find_bin(hist, kTkBins, (uint32_t)p.k, sh);
+  // the first digit's bin; the valid entries are those outside bin 0
+  tk_find_bin<kTkBins / kTkThreads>(hist, (uint32_t)p.k, sh);
+  const uint32_t nvalid = (uint32_t)(rounds * kTkRound) - hist[0];
 
   // radix search for the k-th largest key T; the selection is then key >= T
   uint32_t t_hi = 1u, t_lo = 0u;  // fewer valid entries than k: all of them
   if (nvalid > (uint32_t)p.k) {
-    uint32_t krem = (uint32_t)p.k, pre_hi = 0, msk_hi = 0, pre_lo = 0, msk_lo = 0;
-    for (int dg = 0; dg < 6; ++dg) {
-      const bool lo = dg >= 3;
-      const int shift = dg % 3 == 0 ? 21 : dg % 3 == 1 ? 10 : 0;
-      const int nb = dg % 3 == 2 ? 1024 : 2048;
-      if (dg > 0) {
-        for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
-        __syncthreads();
-        if (staged && !lo) {
-          // a high-word digit over the staged keys: compile-time shifts, one 16-B load per
-          // four keys, an atomic only for the keys still in play (a few per thread)
-          for (int c = 0; c < rounds; ++c) {
-            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + c * kTkRound + 4 * tid);
-            const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (h[e] != 0u && (h[e] & msk_hi) == pre_hi)
-                atomicAdd(&hist[dg == 1 ? (h[e] >> 10) & 2047u : h[e] & 1023u], 1u);
+    const uint32_t b0 = sh.bin;
+    uint32_t krem = (uint32_t)p.k - sh.above;
+    uint32_t pre_hi = b0 << 21, msk_hi = 0xffe00000u, pre_lo = 0, msk_lo = 0;
+    bool done = sh.binh == krem;  // the bin is taken whole
+    bool wide = true;             // the further digits run over every entry
+    if (!done && staged) {
+      // the staged entries in the first digit's bin become the candidates (their staging
+      // index, 16 bits): bit 4c + e of cm is entry c * kTkRound + 4 tid + e
+      uint32_t cm = 0;
+      for (int c = 0; c < rounds; ++c) {
+        const uint4 k4 = *reinterpret_cast<const uint4*>(keys + c * kTkRound + 4 * tid);
+        cm |= ((uint32_t)((k4.x >> 21) == b0) | (uint32_t)((k4.y >> 21) == b0) << 1 |
+               (uint32_t)((k4.z >> 21) == b0) << 2 | (uint32_t)((k4.w >> 21) == b0) << 3)
+              << (4 * c);
+      }
+      uint32_t nc;
+      uint32_t o = tk_scan((uint32_t)__popc(cm), sh.ws, &nc);  // (after every read of hist)
+      if (nc <= (uint32_t)kTkCandCap) {
+        wide = false;
+        uint16_t* cand = reinterpret_cast<uint16_t*>(hist + kTkCandBins);
+        while (cm != 0u) {
+          const int e = __ffs(cm) - 1;
+          cm &= cm - 1u;
+          cand[o++] = (uint16_t)((e >> 2) * kTkRound + 4 * tid + (e & 3));
+        }
+        // digits of 10 bits (the last of each word narrower) over the candidates only
+        for (int dg = 0; dg < 7 && !done; ++dg) {
+          const bool lo = dg >= 3;
+          const int shift = dg == 0 ? 11 : dg == 1 ? 1 : dg == 2 ? 0 : dg == 3 ? 22 : dg == 4 ? 12 : dg == 5 ? 2 : 0;
+          const uint32_t wm = dg == 2 ? 1u : dg == 6 ? 3u : 1023u;
+          for (int i = tid; i < kTkCandBins; i += kTkThreads) hist[i] = 0u;
+          __syncthreads();  // (also orders the candidate writes before their reads)
+          for (int j = tid; j < (int)nc; j += kTkThreads) {
+            const int i = cand[j];
+            const uint32_t h = keys[i];
+            if (!lo) {
+              if ((h & msk_hi) == pre_hi) atomicAdd(&hist[(h >> shift) & wm], 1u);
+            } else if (h == pre_hi) {
+              const uint32_t l = ~(uint32_t)src.gid(i);
+              if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & wm], 1u);
+            }
           }
-        } else {
-          for (int c = 0; c < rounds; ++c) {
-            const uint4 k4 = get4(c);
-            const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+          __syncthreads();
+          tk_find_bin<kTkCandBins / kTkThreads>(hist, krem, sh);
+          krem -= sh.above;
+          if (!lo) {
+            pre_hi |= sh.bin << shift;
+            msk_hi |= wm << shift;
+          } else {
+            pre_lo |= sh.bin << shift;
+            msk_lo |= wm << shift;
+          }
+          done = sh.binh == krem;  // (always by the last digit: keys differ)
+          __syncthreads();  // every thread has read the bin before the histogram is cleared
+        }
+      }
+    }
+    // the further digits over every entry: lists past the staging, or too many candidates
+    for (int dg = 1; dg < 6 && wide && !done; ++dg) {
+      const bool lo = dg >= 3;
+      const int shift = dg % 3 == 1 ? 10 : dg % 3 == 2 ? 0 : 21;
+      const int nb = dg % 3 == 2 ? 1024 : 2048;
+      for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
+      __syncthreads();
+      if (staged && !lo) {
+        // a high-word digit over the staged keys: compile-time shifts, one 16-B load per
+        // four keys, an atomic only for the keys still in play
+        for (int c = 0; c < rounds; ++c) {
+          const uint4 k4 = *reinterpret_cast<const uint4*>(keys + c * kTkRound + 4 * tid);
+          const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (!lo) {
-                hist_add(hist, h[e], msk_hi, pre_hi, shift, nb);
-              } else if (h[e] != 0u && h[e] == pre_hi) {
-                const uint32_t l = ~(uint32_t)src.gid(c * kTkRound + 4 * tid + e);
-                if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
-              }
+          for (int e = 0; e < 4; ++e)
+            if ((h[e] & msk_hi) == pre_hi)
+              atomicAdd(&hist[dg == 1 ? (h[e] >> 10) & 2047u : h[e] & 1023u], 1u);
+        }
+      } else {
+        for (int c = 0; c < rounds; ++c) {
+          const uint4 k4 = get4(c);
+          const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (!lo) {
+              hist_add(hist, h[e], msk_hi, pre_hi, shift, nb);
+            } else if (h[e] == pre_hi) {
+              const uint32_t l = ~(uint32_t)src.gid(c * kTkRound + 4 * tid + e);
+              if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
             }
           }
         }
-        __syncthreads();
       }
-      if (dg > 0) tk_find_bin(hist, nb, krem, sh);
-      const uint32_t b = sh.bin;
+      __syncthreads();
+      if (nb == 2048)
+        tk_find_bin<2048 / kTkThreads>(hist, krem, sh);
+      else
+        tk_find_bin<1024 / kTkThreads>(hist, krem, sh);
       krem -= sh.above;
-      const uint32_t hb = hist[b];
       if (!lo) {
-        pre_hi |= b << shift;
+        pre_hi |= sh.bin << shift;
         msk_hi |= (uint32_t)(nb - 1) << shift;
       } else {
-        pre_lo |= b << shift;
+        pre_lo |= sh.bin << shift;
         msk_lo |= (uint32_t)(nb - 1) << shift;
       }
+      done = sh.binh == krem;
       __syncthreads();  // every thread has read the bin before the histogram is cleared
-      if (hb == krem) break;  // the bin is taken whole (always by the last digit: keys differ)
     }
     t_hi = pre_hi;
     t_lo = pre_lo;
@@ -331,8 +407,8 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
     const int nch = E >> 2, lim = rounds * kTkRound;
     const int e0 = E * tid;
     uint32_t smask = 0;
-    for (int j = 0; j < nch; ++j) {
-      const int jj = (j + tid) % nch;
+    int jj = tid % nch;
+    for (int j = 0; j < nch; ++j, jj = jj + 1 == nch ? 0 : jj + 1) {
       const int i = e0 + 4 * jj;
       if (i >= lim) continue;  // (entries past the staged rounds are past the end: key 0)
       const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
@@ -466,7 +542,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
       // where its pair's two runs stand at the slice start (a merge-path binary search) and
       // merges sequentially from there
       int32_t* src_b = sorted;
-      int32_t* dst_b = sorted + p.kp;
+      int32_t* dst_b = sorted2;
       int nr = p.D;
       const int E = (cnt + kTkThreads - 1) / kTkThreads;
       if (nr == 1) {
@@ -544,7 +620,8 @@ size_t tk_smem_bytes(int stage, int kp) { return (size_t)(kTkBins + stage + kp) 
 
 template <bool MERGE>
 cudaError_t tk_launch(const TopkParams& p, int64_t lists, cudaStream_t st) {
-  const size_t smem = tk_smem_bytes(p.stage, MERGE ? 2 * p.kp : 0);  // merge: two run buffers
+  // merge: two run buffers, past the staging when they do not fit inside (see the kernel)
+  const size_t smem = tk_smem_bytes(p.stage, MERGE && p.kp > kTkBins ? 2 * p.kp : 0);
   cudaError_t e = raise_smem_limit((const void*)topk_kernel<MERGE>, smem);
   if (e != cudaSuccess) return e;
   topk_kernel<MERGE><<<(unsigned)lists, kTkThreads, smem, st>>>(p);

@@ -51,7 +51,7 @@ def _check_local(dcp, sc, ll, k, D, I, shard=-1):
 @pytest.mark.parametrize("D,I,k,stride,ties", [
     (2, 1, 16, 300, False), (3, 1, 40, 257, True), (8, 1, 64, 1000, False),
     (4, 64, 100, 700, True), (1, 1, 1, 50, False), (2, 4, 2048, 5000, False),
-    (8, 1, 300, 16384, True)])
+    (8, 1, 300, 16384, True), (8, 1, 2048, 16384, True), (2, 1, 2048, 16384, False)])
 def test_local_candidates_match_oracle(dcp, D, I, k, stride, ties):
     R = 7
     sc = _scores(D, R, stride, seed=D * 7 + k, ties=ties, masked=0.02, nan=0.01)
