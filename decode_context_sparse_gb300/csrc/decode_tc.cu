@@ -724,12 +724,21 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     // multiplied by 2^(14 - e), e the exponent of their largest magnitude (exact; keeps them
     // in FP16's range), and the head's logits by qs = 2^(e - 14) to undo it.
     float qs = 1.0f;
-    auto load_q = [&](int64_t r) {
+    // Q of unit u (row r); the next unit's rows of Q are prefetched into L2, so that its load,
+    // which the unit's first Q.K^T waits for, does not wait for DRAM.
+    auto load_q = [&](int64_t u, int64_t r) {
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) + (r * H + h) * kDqk);
+      if (h < H && u + 1 < p.num_units) {
+        const int64_t rn = FUSED ? u + 1 : (u + 1) % p.rows;
+        const char* qn = reinterpret_cast<const char*>(p.q) + (rn * H + h) * (kDqk * 2);
+#pragma unroll
+        for (int l = 0; l < 4; ++l) prefetch_l2(qn + crank * 512 + 128 * l);
+        prefetch_l2(qn + 1024);  // the RoPE dims of both CTAs
+      }
       uint32_t mx = 0;  // largest |bf16| bit pattern over this CTA's 288 dims
       if (h < H) {
-#pragma unroll 4
+#pragma unroll 12
         for (int i = 0; i < 36; ++i) {
           const uint4 v = __ldg(src + (i < 32 ? crank * 32 + i : 64 + crank * 4 + (i - 32)));
           const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
@@ -772,7 +781,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     Walk<FUSED, SPARSE> wa;
     wa.init(p, sh.unit0, sh.tile0, ntiles);
     // the pair's first unit, even when it starts mid-unit
-    if (ntiles > 0) load_q(wa.info.r);
+    if (ntiles > 0) load_q(wa.u, wa.info.r);
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
       if (!mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag)) break;
@@ -814,12 +823,6 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_free[buf]);
-      // the next unit's queries go in once this tile's Q.K^T is done
-      if (wa.last() && j + 1 < ntiles) {
-        Walk<FUSED, SPARSE> wn = wa;
-        wn.next(p);
-        load_q(wn.info.r);
-      }
       // this CTA's partial into the local box: read by stage B (free once B(j-1) read it)
       // and copied to the peer's inbox (the warp's 32 rows in one bulk copy, free once the
       // copy of tile j-1 has read them)
@@ -842,6 +845,13 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         bulk_s2peer(xin + (x * 128 + r0) * L::XSTRIDE, xself + (xs * 128 + r0) * L::XSTRIDE,
                     32 * L::XSTRIDE * 4, peer, &sh.in_full[x]);
         bulk_commit();
+      }
+      // the next unit's queries go in once this tile's Q.K^T is done and its partial is on
+      // its way (the next unit's first Q.K^T waits for them; stage B of this tile does not)
+      if (wa.last() && j + 1 < ntiles) {
+        Walk<FUSED, SPARSE> wn = wa;
+        wn.next(p);
+        load_q(wn.u, wn.info.r);
       }
       wa.next(p);
     }

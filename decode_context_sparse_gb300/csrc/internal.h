@@ -71,6 +71,7 @@ struct TopkParams {
   int k;
   int vec;                // lists 16-B aligned with a multiple of 4 entries per row / list
   int stage, kp;          // set by the launchers: staged entries, sort size (merge)
+  FastDiv div;            // set by the launchers: candidates: by I; merge: by stride
   float* cand_score;      // candidates: [n_in][rows][k]
   int32_t* cand_idx;
   int32_t* topk;          // merge: [rows][k]

@@ -9,8 +9,8 @@
 // divided by the scale and rounded to nearest-even E4M3 with saturation at 448 by the
 // hardware conversion; an all-zero block stores scale 0 and zero codes.  RoPE (64 bf16) is
 // copied.  BF16: the 1152-byte row is copied.  HBM-bound: 1152 B read and 656 / 1152 B
-// written per row.  A row's data is loaded before its position and block-table entry are
-// resolved, so the three loads overlap.
+// written per row.  A warp loads its next row (data, position, sequence) before it
+// resolves and writes the current one, so two rows' loads are in flight per warp.
 //
 // The quotients.  With r = 1 / scale correctly rounded, q0 = v * r lies within one ulp of
 // v / scale; the residual e = q0 * scale - v is exact in one fused multiply-add, and

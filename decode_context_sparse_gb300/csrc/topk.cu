@@ -65,17 +65,19 @@ struct TkList {
   int n;               // entries
   int D, I, s;         // candidates: owner rule and shard
   bool vec;            // four consecutive entries from one 16-B aligned load
+  FastDiv div;         // candidates: division by I; merge: by kin
 
   __device__ __forceinline__ int64_t off(int i) const {
     if (!MERGE) return i;
-    const int d = i / kin;
+    const int d = fdiv(i, div);
     return d * dstride + (i - d * kin);
   }
   __device__ __forceinline__ float score(int i) const { return __ldg(sc + off(i)); }
   __device__ __forceinline__ int gid(int i) const {
     if (MERGE) return __ldg(id + off(i));
     if (I == 1) return i * D + s;
-    return (i / I) * I * D + s * I + i % I;  // local slot i of shard s (< 2^31, host-checked)
+    const int q = fdiv(i, div);
+    return q * I * D + s * I + (i - q * I);  // local slot i of shard s (< 2^31, host-checked)
   }
   __device__ __forceinline__ uint32_t key(int i) const {
     if (MERGE && gid(i) < 0) return 0u;
@@ -161,6 +163,7 @@ struct TkShared {
   uint32_t cw[kTkBlockRounds][kTkWarps];   // selected entries per (round, warp) of a block
   uint32_t off[kTkBlockRounds][kTkWarps];  // their output offsets
   uint32_t bin, above, binh, base;  // a digit's bin, the keys in play above it, its count
+  int maxid;                         // merge: the largest selected id
   int run[DCP_MAX_SHARDS + 1];  // merge: first selected entry of each shard's list
 };
 
@@ -199,7 +202,8 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t h, uint32_t ms
 }
 
 template <bool MERGE>
-__global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
+// (three CTAs per SM: 72 KB of shared memory each, at most 42 registers a thread)
+__global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint32_t tk_smem[];
   uint32_t* hist = tk_smem;
   uint32_t* keys = tk_smem + kTkBins;                          // p.stage entries
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
 
   TkList<MERGE> src;
   src.vec = p.vec != 0;
+  src.div = p.div;
   if (MERGE) {
     src.sc = p.score + li * (int64_t)p.stride;
     src.id = p.ids + li * (int64_t)p.stride;
@@ -423,14 +428,28 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
     }
     uint32_t total;
     uint32_t pos = tk_scan((uint32_t)__popc(smask), sh.ws, &total);
+    // candidate lists with k <= kTkBins: the selected entries' indices go to the histogram's
+    // words first, and are written out with consecutive threads on consecutive positions
+    const bool via_smem = !MERGE && p.k <= kTkBins;
+    int32_t* sel = reinterpret_cast<int32_t*>(hist);
     while (smask != 0u && pos < (uint32_t)p.k) {
       const int e = __ffs(smask) - 1;
       smask &= smask - 1u;
       const int i = e0 + e;
-      emit(i, keys[i], pos++);
+      if (via_smem)
+        sel[pos++] = i;
+      else
+        emit(i, keys[i], pos++);
     }
     if (tid == 0) sh.base = total;
     __syncthreads();
+    if (via_smem) {
+      const int ns = (int)min(total, (uint32_t)p.k);
+      for (int j = tid; j < ns; j += kTkThreads) {
+        const int i = sel[j];
+        emit(i, keys[i], (uint32_t)j);
+      }
+    }
   } else {
     // lists past the staging: the keys come from L2, in rounds; a block of kTkBlockRounds
     // rounds at a time: count per (round, warp), one scan, then each warp writes its entries
@@ -521,11 +540,53 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
       }
       sh.run[tid] = lo;
     }
+    if (tid == 0) sh.maxid = -1;
     __syncthreads();
-    for (int j = tid; j < cnt; j += kTkThreads) sorted[j] = src.gid(sorted[j]);
+    int mx = -1;
+    for (int j = tid; j < cnt; j += kTkThreads) {
+      const int id = src.gid(sorted[j]);
+      sorted[j] = id;
+      mx = max(mx, id);
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0 && mx >= 0) atomicMax(&sh.maxid, mx);
     __syncthreads();
-    // runs in increasing id order (as dcp_topk_local writes its lists): place every id by
-    // its rank -- its place in its own run plus the smaller ids of the other runs
+    int32_t* out = p.topk + li * p.k;
+    // ids below 32 x the staging's words: a bitmap of the selected ids over the staging (free
+    // now) gives their increasing order directly -- each thread counts the set bits of its
+    // words, one scan, and writes its ids in order.  Not taken when an id repeats (another
+    // shard's list held it too): then the runs are merged as below.
+    const int nw = (sh.maxid >> 5) + 1;
+    if (runs_inside && sh.maxid >= 0 && nw <= p.stage) {
+      uint32_t* bm = keys;
+      for (int w = tid; w < nw; w += kTkThreads) bm[w] = 0u;
+      __syncthreads();
+      bool dup = false;
+      for (int j = tid; j < cnt; j += kTkThreads) {
+        const int id = sorted[j];
+        const uint32_t bit = 1u << (id & 31);
+        dup |= (atomicOr(&bm[id >> 5], bit) & bit) != 0u;
+      }
+      if (!__syncthreads_or(dup)) {
+        const int W = (nw + kTkThreads - 1) / kTkThreads;
+        const int w0 = min(tid * W, nw), w1 = min(w0 + W, nw);
+        uint32_t c = 0;
+        for (int w = w0; w < w1; ++w) c += __popc(bm[w]);
+        uint32_t total;
+        uint32_t pos = tk_scan(c, sh.ws, &total);
+        for (int w = w0; w < w1; ++w) {
+          uint32_t b = bm[w];
+          while (b != 0u) {
+            out[pos++] = 32 * w + __ffs(b) - 1;
+            b &= b - 1u;
+          }
+        }
+        for (int j = cnt + tid; j < p.k; j += kTkThreads) out[j] = -1;
+        if (tid == 0 && p.count) p.count[li] = cnt;
+        return;
+      }
+    }
+    // runs in increasing id order (as dcp_topk_local writes its lists): merged pairwise
     bool unsorted = false;  // a pair inside a run out of order (pairs across runs may descend)
     for (int j = tid; j + 1 < cnt; j += kTkThreads) {
       int lo = 0, hi = p.D;  // the run of entry j + 1: the last d with run[d] <= j + 1
@@ -535,7 +596,6 @@ __global__ void __launch_bounds__(kTkThreads) topk_kernel(const TopkParams p) {
       }
       unsorted |= sh.run[lo] != j + 1 && sorted[j] >= sorted[j + 1];
     }
-    int32_t* out = p.topk + li * p.k;
     if (!__syncthreads_or(unsorted)) {
       // merge the runs pairwise, ceil(log2 D) levels between sorted[] and a second buffer,
       // the last level into the output: each thread takes a slice of the output, finds
@@ -639,12 +699,14 @@ cudaError_t launch_topk_local(TopkParams p, int n_in, cudaStream_t st) {
   if (p.rows == 0) return cudaSuccess;
   p.stage = tk_stage(p.stride);
   p.kp = 0;
+  p.div = make_fastdiv(p.I);
   return tk_launch<false>(p, p.rows * n_in, st);
 }
 
 cudaError_t launch_topk_merge(TopkParams p, cudaStream_t st) {
   if (p.rows == 0) return cudaSuccess;
   p.stage = tk_stage((int64_t)p.D * p.stride);
+  p.div = make_fastdiv(p.stride);
   int kp = 1;
   while (kp < p.k) kp <<= 1;
   p.kp = kp;
