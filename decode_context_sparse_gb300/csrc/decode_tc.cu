@@ -22,28 +22,30 @@
 //   warp 0      TMEM owner and MMA issuer: S = Q K^T (latent part of Q in TMEM, RoPE part
 //               of Q in shared memory) and O += P V (P in shared memory), each issued as
 //               soon as its inputs are ready;
-//   warps 4-7   converters: staging -> SWIZZLE_128B bf16 K tile (FP8: E4M3 -> bf16,
-//               exact), zero rows for padding, per-slot scales;
+//   warps 4-7   converters: staging -> SWIZZLE_128B FP16 K tile (FP8: E4M3 code times the
+//               power-of-two part of its block scale, exact), zero rows for padding,
+//               per-slot scale factors;
 //   warps 12-15 softmax stage A: thread h owns head h (TMEM lane h): reads its logits of
 //               a tile, scales them, hands this CTA's partial to stage B through a local
 //               box in shared memory and copies the box to the peer CTA's inbox; loads Q;
 //   warps 8-11, 16-19  softmax stage B, two warps per group of 32 heads, each on half of
 //               a tile's columns: adds the two partials, online softmax in base 2 with a
 //               lazily raised reference max (the output is rescaled only when the max
-//               grows by more than 2^8), writes P as bf16 into shared memory, and at the
+//               grows by more than 2^8), writes P as FP16 into shared memory, and at the
 //               end of a row normalises O and writes it out (or a partial of a split row).
 // TMEM columns: O [0,256) | Q latent [256,384) | two logit buffers from 384.  P lives in
 // shared memory, so a logit buffer is free again as soon as stage A has read it.
 //
-// FP8 numerics.  Each CTA's 256 latent dims are two 128-blocks with their own scales
-// s_lo, s_hi, so the logit needs two accumulators: acc_lo = q_lo . k_lo and
-// acc_hi = q_hi . k_hi over the exact E4M3 values.  The RoPE part rides in acc_lo: its
-// keys are stored as k_rope / s_lo split into a bf16 high part and a bf16 remainder
-// (about 16 significant bits), so that s_lo * acc_lo + s_hi * acc_hi is the logit with
-// fp32 accuracy.  (|s_lo| below 2^-60 is taken as 2^-60 for this purpose; the latent
-// term it then adds is below 2^-51 |q|.)  For P V the block scales are folded into P:
-// O[:, lo] += (P s_lo) V_lo, O[:, hi] += (P s_hi) V_hi, with P, s_lo and s_hi rounded to bf16
-// and multiplied as bf16 pairs (one more bf16 rounding of P than a BF16 cache gets).
+// Numerics.  The MMAs take FP16 operands and accumulate in fp32.  Q is multiplied per head by
+// the power of two that puts its largest magnitude in [2^14, 2^15) and the head's logits by
+// the inverse (both exact); BF16 keys are converted to FP16 (exact below 65504).  FP8: each
+// CTA's 256 latent dims are two 128-blocks with scales s = m 2^E (E = floor(log2 s), at most
+// 7; m in [1, 2)).  The K tile holds code * 2^E, exact in FP16, so the logit needs two
+// accumulators, acc_lo and acc_hi, and is m_lo acc_lo + m_hi acc_hi in fp32.  The RoPE part
+// rides in acc_lo: its keys are stored as k_rope / m_lo split into an FP16 high part and an
+// FP16 remainder.  For P V the multipliers are folded into P: O[:, lo] += (P m_lo) V_lo,
+// O[:, hi] += (P m_hi) V_hi, each P m rounded once to FP16 (relative error 2^-11).  A block
+// whose scale is 0 or below 2^-24 counts as zero.
 //
 // Work: a persistent grid of pairs; the concatenated sequence of 32-slot tiles of all
 // units (rows, or (shard, row) pairs) is cut into equal contiguous ranges, one per pair.
