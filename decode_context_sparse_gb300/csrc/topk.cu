@@ -276,67 +276,83 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
   // the first digit's bin; the valid entries are those outside bin 0
   tk_find_bin<kTkBins / kTkThreads>(hist, (uint32_t)p.k, sh);
   const uint32_t nvalid = (uint32_t)(rounds * kTkRound) - hist[0];
+  // more valid entries than k: a radix search for the k-th largest key T, the selection
+  // being key >= T; else every valid entry (key >= 1)
+  const bool search = nvalid > (uint32_t)p.k;
+  const uint32_t b0 = search ? sh.bin : 0u;
+  uint32_t krem = search ? (uint32_t)p.k - sh.above : 0u;
+  bool done = !search || sh.binh == krem;  // (a bin taken whole ends the search)
+  uint32_t pre_hi = search ? b0 << 21 : 1u, msk_hi = 0xffe00000u, pre_lo = 0, msk_lo = 0;
 
-  // radix search for the k-th largest key T; the selection is then key >= T
-  uint32_t t_hi = 1u, t_lo = 0u;  // fewer valid entries than k: all of them
-  if (nvalid > (uint32_t)p.k) {
-    const uint32_t b0 = sh.bin;
-    uint32_t krem = (uint32_t)p.k - sh.above;
-    uint32_t pre_hi = b0 << 21, msk_hi = 0xffe00000u, pre_lo = 0, msk_lo = 0;
-    bool done = sh.binh == krem;  // the bin is taken whole
-    bool wide = true;             // the further digits run over every entry
-    if (!done && staged) {
-      // the staged entries in the first digit's bin become the candidates (their staging
-      // index, 16 bits): bit 4c + e of cm is entry c * kTkRound + 4 tid + e
-      uint32_t cm = 0;
-      for (int c = 0; c < rounds; ++c) {
-        const uint4 k4 = *reinterpret_cast<const uint4*>(keys + c * kTkRound + 4 * tid);
-        cm |= ((uint32_t)((k4.x >> 21) == b0) | (uint32_t)((k4.y >> 21) == b0) << 1 |
-               (uint32_t)((k4.z >> 21) == b0) << 2 | (uint32_t)((k4.w >> 21) == b0) << 3)
-              << (4 * c);
-      }
-      uint32_t nc;
-      uint32_t o = tk_scan((uint32_t)__popc(cm), sh.ws, &nc);  // (after every read of hist)
-      if (nc <= (uint32_t)kTkCandCap) {
-        wide = false;
-        uint16_t* cand = reinterpret_cast<uint16_t*>(hist + kTkCandBins);
-        while (cm != 0u) {
-          const int e = __ffs(cm) - 1;
-          cm &= cm - 1u;
-          cand[o++] = (uint16_t)((e >> 2) * kTkRound + 4 * tid + (e & 3));
+  // staged lists: one pass over this thread's run of 32 entries [32 tid, 32 tid + 32) (read
+  // in a rotated chunk order, so that the threads of a warp hit distinct banks) sorts them
+  // into those above the first digit's bin (selected whatever T is) and those in it (the
+  // candidates); bit b of a mask is entry 32 tid + b
+  const int e0 = 32 * tid, lim = rounds * kTkRound;
+  uint32_t amask = 0u, cmask = 0u;
+  if (staged) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int jj = (j + tid) & 7;
+      const int i = e0 + 4 * jj;
+      if (i < lim) {  // (entries past the staged rounds are past the end)
+        const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
+        const uint32_t d[4] = {k4.x >> 21, k4.y >> 21, k4.z >> 21, k4.w >> 21};
+        uint32_t a4 = 0u, c4 = 0u;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          a4 |= (uint32_t)(d[e] > b0) << e;
+          c4 |= (uint32_t)(d[e] == b0) << e;
         }
-        // digits of 10 bits (the last of each word narrower) over the candidates only
-        for (int dg = 0; dg < 7 && !done; ++dg) {
-          const bool lo = dg >= 3;
-          const int shift = dg == 0 ? 11 : dg == 1 ? 1 : dg == 2 ? 0 : dg == 3 ? 22 : dg == 4 ? 12 : dg == 5 ? 2 : 0;
-          const uint32_t wm = dg == 2 ? 1u : dg == 6 ? 3u : 1023u;
-          for (int i = tid; i < kTkCandBins; i += kTkThreads) hist[i] = 0u;
-          __syncthreads();  // (also orders the candidate writes before their reads)
-          for (int j = tid; j < (int)nc; j += kTkThreads) {
-            const int i = cand[j];
-            const uint32_t h = keys[i];
-            if (!lo) {
-              if ((h & msk_hi) == pre_hi) atomicAdd(&hist[(h >> shift) & wm], 1u);
-            } else if (h == pre_hi) {
-              const uint32_t l = ~(uint32_t)src.gid(i);
-              if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & wm], 1u);
-            }
-          }
-          __syncthreads();
-          tk_find_bin<kTkCandBins / kTkThreads>(hist, krem, sh);
-          krem -= sh.above;
-          if (!lo) {
-            pre_hi |= sh.bin << shift;
-            msk_hi |= wm << shift;
-          } else {
-            pre_lo |= sh.bin << shift;
-            msk_lo |= wm << shift;
-          }
-          done = sh.binh == krem;  // (always by the last digit: keys differ)
-          __syncthreads();  // every thread has read the bin before the histogram is cleared
-        }
+        amask |= a4 << (4 * jj);
+        cmask |= c4 << (4 * jj);
       }
     }
+    if (!search) cmask = 0u;  // (bin 0: the invalid entries)
+  }
+  bool wide = !staged;  // the further digits run over every entry
+  if (!done && staged) {
+    // the candidates' 16-bit staging indices go to the histogram's upper words
+    uint32_t nc;
+    uint32_t o = tk_scan((uint32_t)__popc(cmask), sh.ws, &nc);  // (after every read of hist)
+    if (nc <= (uint32_t)kTkCandCap) {
+      uint16_t* cand = reinterpret_cast<uint16_t*>(hist + kTkCandBins);
+      for (uint32_t m = cmask; m != 0u; m &= m - 1u) cand[o++] = (uint16_t)(e0 + __ffs(m) - 1);
+      // digits of 10 bits (the last of each word narrower) over the candidates only
+      for (int dg = 0; dg < 7 && !done; ++dg) {
+        const bool lo = dg >= 3;
+        const int shift = dg == 0 ? 11 : dg == 1 ? 1 : dg == 2 ? 0 : dg == 3 ? 22 : dg == 4 ? 12 : dg == 5 ? 2 : 0;
+        const uint32_t wm = dg == 2 ? 1u : dg == 6 ? 3u : 1023u;
+        for (int i = tid; i < kTkCandBins; i += kTkThreads) hist[i] = 0u;
+        __syncthreads();  // (also orders the candidate writes before their reads)
+        for (int j = tid; j < (int)nc; j += kTkThreads) {
+          const int i = cand[j];
+          const uint32_t h = keys[i];
+          if (!lo) {
+            if ((h & msk_hi) == pre_hi) atomicAdd(&hist[(h >> shift) & wm], 1u);
+          } else if (h == pre_hi) {
+            const uint32_t l = ~(uint32_t)src.gid(i);
+            if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & wm], 1u);
+          }
+        }
+        __syncthreads();
+        tk_find_bin<kTkCandBins / kTkThreads>(hist, krem, sh);
+        krem -= sh.above;
+        if (!lo) {
+          pre_hi |= sh.bin << shift;
+          msk_hi |= wm << shift;
+        } else {
+          pre_lo |= sh.bin << shift;
+          msk_lo |= wm << shift;
+        }
+        done = sh.binh == krem;  // (always by the last digit: keys differ)
+        __syncthreads();  // every thread has read the bin before the histogram is cleared
+      }
+    } else {
+      wide = true;
+    }
+  }
+  if (search) {
     // the further digits over every entry: lists past the staging, or too many candidates
     for (int dg = 1; dg < 6 && wide && !done; ++dg) {
       const bool lo = dg >= 3;
@@ -386,9 +402,8 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
       done = sh.binh == krem;
       __syncthreads();  // every thread has read the bin before the histogram is cleared
     }
-    t_hi = pre_hi;
-    t_lo = pre_lo;
   }
+  const uint32_t t_hi = pre_hi, t_lo = pre_lo;
 
   auto selected = [&](uint32_t h, int i) -> bool {
     return h != 0u && (h > t_hi || (h == t_hi && (t_lo == 0u || ~(uint32_t)src.gid(i) >= t_lo)));
@@ -405,27 +420,13 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
     }
   };
   if (staged) {
-    // stable compaction, each thread over a contiguous run of E <= 32 entries (read in a
-    // rotated chunk order: the threads of a warp hit distinct banks): its selection mask,
-    // one block scan of the counts, then its entries written in order
-    const int E = ((n + kTkThreads - 1) / kTkThreads + 3) & ~3;
-    const int nch = E >> 2, lim = rounds * kTkRound;
-    const int e0 = E * tid;
-    uint32_t smask = 0;
-    int jj = tid % nch;
-    for (int j = 0; j < nch; ++j, jj = jj + 1 == nch ? 0 : jj + 1) {
-      const int i = e0 + 4 * jj;
-      if (i >= lim) continue;  // (entries past the staged rounds are past the end: key 0)
-      const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
-      uint32_t m4;
-      if (no_ties)
-        m4 = (uint32_t)(k4.x >= t_hi) | (uint32_t)(k4.y >= t_hi) << 1 |
-             (uint32_t)(k4.z >= t_hi) << 2 | (uint32_t)(k4.w >= t_hi) << 3;
-      else
-        m4 = (uint32_t)selected(k4.x, i) | (uint32_t)selected(k4.y, i + 1) << 1 |
-             (uint32_t)selected(k4.z, i + 2) << 2 | (uint32_t)selected(k4.w, i + 3) << 3;
-      smask |= m4 << (4 * jj);
+    // the candidates that reach T join the entries above the first digit's bin; then a
+    // stable compaction: one block scan of the counts, each thread's entries in order
+    for (uint32_t m = cmask; m != 0u; m &= m - 1u) {
+      const int b = __ffs(m) - 1;
+      if (selected(keys[e0 + b], e0 + b)) amask |= 1u << b;
     }
+    uint32_t smask = amask;
     uint32_t total;
     uint32_t pos = tk_scan((uint32_t)__popc(smask), sh.ws, &total);
     // candidate lists with k <= kTkBins: the selected entries' indices go to the histogram's
