@@ -265,6 +265,119 @@ def time_topk_producer(dcp, dev, peaks, stream, flush, steps, seqs=64):
             "launches_per_call": 2}
 
 
+def _timed_us(stream, flush, fn, steps, fill):
+    """Mean device time of fn in µs: fn is recorded once into a CUDA graph, which is replayed
+    max(3, steps) times after 3 warm-up replays, each replay timed with CUDA events on the
+    launching stream and preceded by an L2 flush (the graph keeps the binding's host-side
+    work out of the timing of the small configurations)."""
+    fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(stream.device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            fn()
+    stream.wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(max(3, steps))]
+    for a, b in ev:
+        flush.fill_(fill)
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def time_configs(dcp, dev, peaks, stream, flush, steps):
+    """Every synthetic configuration of the hot path at N = 1 besides the headline one: the
+    decode configurations (tiny dense BF16, sparse top-k 512 BF16, long dense BF16) fused and
+    unfused (remap or local lengths -> per-shard partials -> merge), with rows/s, µs per call
+    (one layer) and the fraction of the roofline max(gathered KV bytes / HBM peak, FLOPs /
+    tensor peak); and the remap + merge stress at D = 2, 4, 8 against HBM.  Inputs as the
+    parity tests draw them; each call replayed from a CUDA graph, L2 flushed before it."""
+    import synth
+    res = {}
+    for name, make in (("cfg1_tiny_dense_bf16", synth.cfg1_tiny_dense),
+                       ("cfg2_sparse_topk512_bf16", synth.cfg2_sparse_topk512),
+                       ("cfg5_dense_long_bf16", synth.cfg5_dense_long)):
+        g = make(device=dev)
+        R, H, D, I = g.rows, g.heads, g.dcp, g.interleave
+        if g.topk is not None:
+            slots = int((g.topk >= 0).sum().item())
+            kw = dict(idx=g.topk)
+        else:
+            slots = int(g.row_len.sum().item())
+            kw = dict(kv_len=g.row_len, max_kv_len=int(g.row_len.max().item()))
+            ll = dcp.dcp_local_lengths(g.row_len, D, I)
+        out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+        po = torch.empty((D, R, H, 512), dtype=torch.float32, device=dev)
+        pl = torch.empty((D, R, H), dtype=torch.float32, device=dev)
+        loc = torch.empty((D, R, max(g.k, 1)), dtype=torch.int32, device=dev)
+        cnt = torch.empty((D, R), dtype=torch.int32, device=dev)
+
+        def fused():
+            dcp.mla_decode_dcp_fused(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq,
+                                     g.sm_scale, D, I, out=out, lse=lse, **kw)
+
+        def unfused():
+            if g.topk is not None:
+                dcp.dcp_remap_topk(g.topk, D, I, local_idx=loc, count=cnt)
+                dcp.mla_decode_partial_lse(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq,
+                                           g.sm_scale, idx=loc, count=cnt, num_shards=D,
+                                           out=po, lse=pl)
+            else:
+                dcp.mla_decode_partial_lse(g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq,
+                                           g.sm_scale, kv_len=ll, max_kv_len=kw["max_kv_len"],
+                                           num_shards=D, out=po, lse=pl)
+            dcp.dcp_lse_merge(po, pl, out=out, lse=lse)
+
+        us_f = _timed_us(stream, flush, fused, steps, 6)
+        us_u = _timed_us(stream, flush, unfused, steps, 7)
+        kv_bytes = slots * g.token_bytes
+        flops = slots * 2 * H * (576 + 512)
+        t_hbm = kv_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+        t_tc = flops / (peaks["bf16_tflops"] * 1e12) * 1e6
+        roof = max(t_hbm, t_tc)
+        res[name] = {"rows": R, "heads": H, "dcp": D, "kv_slots": slots,
+                     "kernel": "tensor cores" if 48 <= H <= 128 else "CUDA cores",
+                     "fused": {"us": us_f, "rows_per_s": R / (us_f / 1e6),
+                               "roofline_frac": roof / us_f},
+                     "unfused": {"us": us_u, "rows_per_s": R / (us_u / 1e6),
+                                 "roofline_frac": roof / us_u},
+                     "bound": "tensor" if t_tc >= t_hbm else "hbm", "roofline_us": roof,
+                     "algorithmic_bytes": kv_bytes, "flops": flops}
+        del g
+    stress = {}
+    for D in (2, 4, 8):
+        m = synth.cfg4_remap_merge(D, device=dev)
+        R, K = m.topk.shape
+        H = m.part_out.shape[2]
+        loc = torch.empty((D, R, K), dtype=torch.int32, device=dev)
+        cnt = torch.empty((D, R), dtype=torch.int32, device=dev)
+        out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+        us_r = _timed_us(stream, flush, lambda: dcp.dcp_remap_topk(
+            m.topk, D, m.interleave, local_idx=loc, count=cnt), steps, 8)
+        us_m = _timed_us(stream, flush, lambda: dcp.dcp_lse_merge(
+            m.part_out, m.part_lse, out=out, lse=lse), steps, 9)
+        b_r = R * K * 4 + D * R * K * 4 + D * R * 4
+        b_m = D * R * H * (512 + 1) * 4 + R * H * (512 * 2 + 4)
+        stress["dcp%d" % D] = {
+            "remap_us": us_r, "remap_gbs": b_r / (us_r / 1e6) / 1e9,
+            "merge_us": us_m, "merge_gbs": b_m / (us_m / 1e6) / 1e9,
+            "merge_frac": b_m / (us_m / 1e6) / 1e9 / peaks["hbm_gbs"],
+            "remap_bytes": b_r, "merge_bytes": b_m}
+        del m
+    res["cfg4_remap_merge_stress"] = dict(stress, rows=256, k=2048, heads=128,
+                                          interleave="page (64)", bound="hbm")
+    return res
+
+
 def time_prefill_chunk(dcp, dev, peaks, stream, flush, steps):
     """A chunked-prefill step of the same model shapes: 2 sequences x 64 chunk tokens after a
     16384-token cached prefix, 128 heads, FP8, D = 8.  Timed as the prefix + chunk partials
@@ -522,6 +635,7 @@ def main():
     topk_prod = time_topk_producer(dcp, dev, peaks, stream, flush, args.steps)
     prefill = time_prefill_chunk(dcp, dev, peaks, stream, flush, args.steps)
     graph_step = time_graph_step(dcp, dev)
+    configs = time_configs(dcp, dev, peaks, stream, flush, args.steps)
 
     # end to end through the public API with host buffers: H2D of the step's inputs (queries,
     # top-k ids, row map, block tables) from pinned memory, D2H of the outputs
@@ -671,6 +785,7 @@ def main():
         "topk_producer": topk_prod,
         "prefill_chunk": prefill,
         "graph_step": graph_step,
+        "configs": configs,
         "clocks": clocks,
         "e2e": {"value": e2e_val, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": pipe_ms / args.steps,

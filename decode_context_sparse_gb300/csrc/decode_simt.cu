@@ -346,7 +346,7 @@ int simt_auto_splits(int64_t units, int heads, int64_t max_tokens) {
   const int64_t ctas = units * (heads / kHG);
   const int64_t target = 152 * 4;
   int64_t s = (target + ctas - 1) / ctas;
-  const int64_t by_len = (max_tokens + 127) / 128;  // at least 128 slots per split
+  const int64_t by_len = (max_tokens + kTile - 1) / kTile;  // at least one tile per split
   s = s < by_len ? s : by_len;
   if (s < 1) s = 1;
   if (s > 64) s = 64;
