@@ -915,41 +915,65 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       const float fix = ltot > 0.f ? 1.0f / ltot : 0.f;
       const float lse_v = ltot > 0.f ? (m_ref + __log2f(ltot)) * kLn2 : -INFINITY;
       const int64_t u = w.u;
-      const int64_t oi = (u * H + h) * kDv + crank * 256;
       float* wso = p.tc_o + (((int64_t)pair * 2 + slot_idx) * 128 + h) * kDv + crank * 256;
-      // this half's eight 16-column chunks, four per TMEM wait
-      for (int c4 = half * 8; c4 < half * 8 + 8; c4 += 4) {
-        uint32_t v[4][16];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld16(trow + kColO + 16 * (c4 + k), v[k]);
+      // This half's 128 O columns in four rounds of 32.  A split partial goes straight to the
+      // workspace.  A finished unit goes through shared memory so that the global stores are
+      // row-contiguous: each lane puts its head's 32 values into its row of this half's chunks
+      // of the two P buffers (both free: P.V of this unit's last tile is done, and each half
+      // uses only the chunks it writes P into), then the warp stores 4 heads (fp32) or 8 heads
+      // (bf16) per instruction, 128 or 64 contiguous bytes each.
+      unsigned char* pst = smem + L::OFF_P;
+      auto stage_addr = [&](int r, int k) -> unsigned char* {  // row r, float4 k of 8
+        const int cc = (k & 3) < 2 ? 2 * half + (k & 3) : 4 + 2 * half + (k & 3) - 2;
+        return pst + (k >> 2) * L::P_BYTES + (r >> 3) * 1024 + (r & 7) * 128 +
+               ((cc ^ (r & 7)) << 4);
+      };
+#pragma unroll 1
+      for (int rc = 0; rc < 4; ++rc) {
+        const int c0 = half * 8 + 2 * rc;  // first 16-column chunk of this round
+        uint32_t v[2][16];
+        tmem_ld16(trow + kColO + 16 * c0, v[0]);
+        tmem_ld16(trow + kColO + 16 * (c0 + 1), v[1]);
         tmem_ld_wait();
+        float f[32];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = c4 + k;
-          float f[16];
+        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i >> 4][i & 15]) * fix;
+        if (!complete) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[k][i]) * fix;
-          if (!complete) {
+          for (int i = 0; i < 8; ++i)
+            __stcg(reinterpret_cast<float4*>(wso + 16 * c0) + i,
+                   make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]));
+          continue;
+        }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              __stcg(reinterpret_cast<float4*>(wso + 16 * c) + i,
-                     make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]));
-          } else if (h < H) {
-            if (FUSED) {
-              uint32_t b2[8];
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<float4*>(stage_addr(h, k)) =
+              make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+        __syncwarp();
+        const int64_t col = crank * 256 + 16 * c0;  // first output column of the round
+        if (FUSED) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) b2[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-              uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi + 16 * c);
-              o[0] = make_uint4(b2[0], b2[1], b2[2], b2[3]);
-              o[1] = make_uint4(b2[4], b2[5], b2[6], b2[7]);
-            } else {
-              float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + oi + 16 * c);
+          for (int i = 0; i < 4; ++i) {
+            const int r = grp * 32 + 8 * i + (lane >> 2), q = lane & 3;
+            const float4 a = *reinterpret_cast<const float4*>(stage_addr(r, 2 * q));
+            const float4 b = *reinterpret_cast<const float4*>(stage_addr(r, 2 * q + 1));
+            if (r < H)
+              *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) +
+                                        (u * H + r) * kDv + col + 8 * q) =
+                  make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                             pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+          }
+        } else {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                o[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-            }
+          for (int i = 0; i < 8; ++i) {
+            const int r = grp * 32 + 4 * i + (lane >> 3), q = lane & 7;
+            const float4 a = *reinterpret_cast<const float4*>(stage_addr(r, q));
+            if (r < H)
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (u * H + r) * kDv +
+                                         col + 4 * q) = a;
           }
         }
+        __syncwarp();  // the rows are read before the next round overwrites them
       }
       tc_fence_before();
       if (complete) {
