@@ -73,6 +73,8 @@ int prepare_decode(const dcp_mla_decode_args* a, int32_t n, bool fused, int32_t 
   p.I = fused ? interleave : 1;
   p.rule = make_owner_rule(p.D, p.I);
   p.num_units = units;
+  p.shards = fused ? 1 : n;
+  p.shards_div = make_fastdiv(p.shards);
   p.num_splits = splits;
   p.out = a->out;
   p.lse = a->lse;

@@ -139,7 +139,7 @@ struct TcShared {
   int abort_flag;
   int64_t T, t0;
   int Peff;  // pairs that own tiles: min(pairs, T), so no pair's range is empty
-  int64_t unit0;
+  int64_t unit0;  // order index of the pair's first unit
   int tile0, ntiles;
   int64_t scan_base;
 };
@@ -147,37 +147,48 @@ struct TcShared {
 static_assert(TcLay<DCP_KV_FP8_E4M3_S128>::SMEM + sizeof(TcShared) <= 232448, "shared memory");
 static_assert(TcLay<DCP_KV_BF16>::SMEM + sizeof(TcShared) <= 232448, "shared memory");
 
+// A unit: a row (fused) or a (shard, row) pair (partial), whose id u indexes the caller's
+// [shards][rows] arrays.  The kernel visits the partial form's units row by row, the shards
+// of one row one after another (order index v = row * shards + shard), so that consecutive
+// units share the row's queries and the Q load is skipped between them.
 struct UnitInfo {
-  int64_t r;
+  int64_t u, r;
   int shard, b, n, ntile;
 };
 
+template <bool FUSED>
+__device__ __forceinline__ int64_t unit_row(const DecodeParams& p, int64_t v) {
+  return FUSED ? v : fdiv((int)v, p.shards_div);
+}
+
 template <bool FUSED, bool SPARSE>
-__device__ __forceinline__ UnitInfo get_unit(const DecodeParams& p, int64_t u) {
+__device__ __forceinline__ UnitInfo get_unit(const DecodeParams& p, int64_t v) {
   UnitInfo x;
-  x.r = FUSED ? u : u % p.rows;
-  x.shard = FUSED ? 0 : (int)(u / p.rows);
+  x.r = unit_row<FUSED>(p, v);
+  x.shard = FUSED ? 0 : (int)(v - x.r * p.shards);
+  x.u = FUSED ? v : (int64_t)x.shard * p.rows + x.r;
   x.b = __ldg(p.row_seq + x.r);
   if (SPARSE)
-    x.n = FUSED ? p.k : min(max(__ldg(p.count + u), 0), p.k);
+    x.n = FUSED ? p.k : min(max(__ldg(p.count + x.u), 0), p.k);
   else
-    x.n = max(0, __ldg(p.kv_len + u));
+    x.n = max(0, __ldg(p.kv_len + x.u));
   if (x.b < 0 || x.b >= p.num_seqs) x.n = 0;
   x.ntile = (x.n + kTN - 1) / kTN;
   return x;
 }
 
-// Walk over this pair's tiles, unit by unit (empty units contribute no tiles).
+// Walk over this pair's tiles, unit by unit in visiting order (empty units contribute no
+// tiles); v is the order index, info.u the unit's id.
 template <bool FUSED, bool SPARSE>
 struct Walk {
-  int64_t u;
+  int64_t v;
   int lt, left;
   UnitInfo info;
-  __device__ void init(const DecodeParams& p, int64_t u0, int tile0, int ntiles) {
-    u = u0;
+  __device__ void init(const DecodeParams& p, int64_t v0, int tile0, int ntiles) {
+    v = v0;
     lt = tile0;
     left = ntiles;
-    if (left > 0) info = get_unit<FUSED, SPARSE>(p, u);
+    if (left > 0) info = get_unit<FUSED, SPARSE>(p, v);
   }
   __device__ bool first() const { return lt == 0; }
   __device__ bool last() const { return lt == info.ntile - 1; }
@@ -185,8 +196,8 @@ struct Walk {
     if (--left <= 0) return;
     if (++lt == info.ntile) {
       do {
-        ++u;
-        info = get_unit<FUSED, SPARSE>(p, u);
+        ++v;
+        info = get_unit<FUSED, SPARSE>(p, v);
       } while (info.ntile == 0);
       lt = 0;
     }
@@ -323,7 +334,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     }
   } else {
     int64_t part = 0;
-    for (int64_t u = tid; u < U; u += kTcThreads) part += get_unit<FUSED, SPARSE>(p, u).ntile;
+    for (int64_t v = tid; v < U; v += kTcThreads) part += get_unit<FUSED, SPARSE>(p, v).ntile;
     int64_t T;
     block_scan_excl(part, scan_tmp, &T);
     const int Pe = (int)(T < P ? (T > 0 ? T : 1) : P);
@@ -340,12 +351,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     __syncthreads();
     if (t1 > t0) {
       for (int64_t c0 = 0; c0 < U; c0 += kTcThreads) {
-        const int64_t u = c0 + tid;
-        const int nt = u < U ? get_unit<FUSED, SPARSE>(p, u).ntile : 0;
+        const int64_t v = c0 + tid;  // order index
+        const int nt = v < U ? get_unit<FUSED, SPARSE>(p, v).ntile : 0;
         int64_t chunk_total;
         const int64_t excl = block_scan_excl(nt, scan_tmp, &chunk_total) + sh.scan_base;
         if (nt > 0 && t0 >= excl && t0 < excl + nt) {
-          sh.unit0 = u;
+          sh.unit0 = v;
           sh.tile0 = (int)(t0 - excl);
         }
         __syncthreads();
@@ -471,7 +482,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         if (pos < wi.info.n) {
           n_has = true;
           if (SPARSE) {
-            const int64_t base = FUSED ? wi.info.r * (int64_t)p.k : wi.u * (int64_t)p.k;
+            const int64_t base = (FUSED ? wi.info.r : wi.info.u) * (int64_t)p.k;
             n_v = __ldg(p.idx + base + pos);  // consumed in stage T
           } else {
             n_v = pos;
@@ -726,14 +737,13 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     // multiplied by 2^(14 - e), e the exponent of their largest magnitude (exact; keeps them
     // in FP16's range), and the head's logits by qs = 2^(e - 14) to undo it.
     float qs = 1.0f;
-    // Q of unit u (row r); the next unit's rows of Q are prefetched into L2, so that its load,
-    // which the unit's first Q.K^T waits for, does not wait for DRAM.
-    auto load_q = [&](int64_t u, int64_t r) {
+    // Q of row r; the next row's Q is prefetched into L2, so that its load, which that row's
+    // first Q.K^T waits for, does not wait for DRAM.
+    auto load_q = [&](int64_t r) {
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) + (r * H + h) * kDqk);
-      if (h < H && u + 1 < p.num_units) {
-        const int64_t rn = FUSED ? u + 1 : (u + 1) % p.rows;
-        const char* qn = reinterpret_cast<const char*>(p.q) + (rn * H + h) * (kDqk * 2);
+      if (h < H && r + 1 < p.rows) {
+        const char* qn = reinterpret_cast<const char*>(p.q) + ((r + 1) * H + h) * (kDqk * 2);
 #pragma unroll
         for (int l = 0; l < 4; ++l) prefetch_l2(qn + crank * 512 + 128 * l);
         prefetch_l2(qn + 1024);  // the RoPE dims of both CTAs
@@ -783,7 +793,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     Walk<FUSED, SPARSE> wa;
     wa.init(p, sh.unit0, sh.tile0, ntiles);
     // the pair's first unit, even when it starts mid-unit
-    if (ntiles > 0) load_q(wa.u, wa.info.r);
+    if (ntiles > 0) load_q(wa.info.r);
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
       if (!mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag)) break;
@@ -849,11 +859,17 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         bulk_commit();
       }
       // the next unit's queries go in once this tile's Q.K^T is done and its partial is on
-      // its way (the next unit's first Q.K^T waits for them; stage B of this tile does not)
+      // its way (the next unit's first Q.K^T waits for them; stage B of this tile does not);
+      // the next shard's unit of the same row keeps them
       if (wa.last() && j + 1 < ntiles) {
         Walk<FUSED, SPARSE> wn = wa;
         wn.next(p);
-        load_q(wn.u, wn.info.r);
+        if (wn.info.r != wa.info.r) {
+          load_q(wn.info.r);
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.q_ready);
+        }
       }
       wa.next(p);
     }
@@ -876,9 +892,10 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
 
     // units without any slot: zero output, -inf LSE
     if (!(FUSED && SPARSE) && half == 0) {
-      for (int64_t u = pair; u < U; u += P) {
-        const UnitInfo x = get_unit<FUSED, SPARSE>(p, u);
+      for (int64_t v = pair; v < U; v += P) {
+        const UnitInfo x = get_unit<FUSED, SPARSE>(p, v);
         if (x.ntile != 0 || h >= H) continue;
+        const int64_t u = x.u;
         const int64_t oi = (u * H + h) * kDv + crank * 256;
         if (FUSED) {
           uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + oi);
@@ -914,7 +931,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       tc_fence_after();
       const float fix = ltot > 0.f ? 1.0f / ltot : 0.f;
       const float lse_v = ltot > 0.f ? (m_ref + __log2f(ltot)) * kLn2 : -INFINITY;
-      const int64_t u = w.u;
+      const int64_t u = w.info.u;
       float* wso = p.tc_o + (((int64_t)pair * 2 + slot_idx) * 128 + h) * kDv + crank * 256;
       // This half's 128 O columns in four rounds of 32.  A split partial goes straight to the
       // workspace.  A finished unit goes through shared memory so that the global stores are

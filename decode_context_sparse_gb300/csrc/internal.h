@@ -30,6 +30,8 @@ struct DecodeParams {
   int D, I;               // fused: owner rule
   OwnerRule rule;         // the same as fast divisions
   int64_t num_units;      // partial: shards * rows; fused: rows
+  int shards;             // partial: shards of the call (units per row); fused: 1
+  FastDiv shards_div;     // division by shards
   int num_splits;
   void* out;              // partial: fp32 [units][H][512]; fused: bf16 [rows][H][512]
   float* lse;
