@@ -1060,15 +1060,15 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
           for (int t = 0; t < w2; ++t) r[t] = fmaxf(r[t], r[t + w2]);
         mh = r[0];
       }
-      // every inbox value of this warp has been loaded and used (the max depends on all of
-      // them): hand the rows back to the peer now; a relaxed arrive suffices
-      asm volatile("" ::"f"(mh) : "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_relaxed(&sh.out_free[x], peer);
-      // the row max of the whole tile: the two halves post theirs and read the other's
+      // the row max of the whole tile: the two halves post theirs and read the other's; every
+      // inbox value of this warp has been loaded and used (the max depends on all of them),
+      // so the rows go back to the peer at the same time (a relaxed arrive suffices)
       sh.bx[half][x][h] = mh;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.bx_full[grp][x]);
+      if (lane == 0) {
+        mbar_arrive_cluster_relaxed(&sh.out_free[x], peer);
+        mbar_arrive(&sh.bx_full[grp][x]);
+      }
       if (!(ok = mbar_wait(&sh.bx_full[grp][x], (j >> 1) & 1, abort_flag))) break;
       const float mt = fmaxf(mh, sh.bx[half ^ 1][x][h]);
       // per head: raise the reference when the tile max exceeds it by more than 2^8; the
@@ -1077,7 +1077,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       float alpha = 1.0f;
       const bool raise = mt > m_ref + 8.0f;
       if (raise && m_ref != -INFINITY) alpha = fast_exp2(m_ref - mt);
-      if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
+      if (rescale) {
         if (!(ok = mbar_wait(&sh.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         for (int c = half * 8; c < half * 8 + 8; ++c) {
@@ -1140,8 +1141,8 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
               make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
         }
       }
-      fence_proxy_async_smem();  // P is read by the tensor pipe
-      tmem_st_wait();            // (an O rescale above must land before P.V(j) accumulates)
+      fence_proxy_async_smem();        // P is read by the tensor pipe
+      if (rescale) tmem_st_wait();     // (the O rescale must land before P.V(j) accumulates)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.p_full[j & 1]);
