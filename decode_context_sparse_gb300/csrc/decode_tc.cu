@@ -253,6 +253,60 @@ __device__ __forceinline__ uint32_t fp8_block_mul(float s) {
   return h | (h << 16);
 }
 
+// Q of one (row, head) for a CTA of a pair, as FP16: the CTA's 256 latent dims into TMEM
+// (two per column, at taddr), its 32 RoPE dims into row h of the SW128 A-operand tile qr.
+// The values are multiplied by 2^(14 - e), e the exponent of their largest magnitude (exact;
+// keeps them in FP16's range); returns 2^(e - 14), the factor that undoes it on the logits.
+// Two passes over the 36 16-B pieces (the largest magnitude, then the conversion), each
+// with twelve or eight loads in flight.  Not inlined: it runs once per row, and the warps
+// that call it keep their registers for the per-tile work.
+__device__ __noinline__ float tc_load_q(const uint4* __restrict__ src, bool valid, int crank,
+                                        uint32_t taddr, unsigned char* qr, int hrow) {
+  uint32_t mx = 0;  // largest |bf16| bit pattern over the CTA's 288 dims
+  if (valid) {
+#pragma unroll 12
+    for (int i = 0; i < 36; ++i) {
+      const uint4 v = __ldg(src + (i < 32 ? crank * 32 + i : 64 + crank * 4 + (i - 32)));
+      const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
+                             v.w & 0x7fff7fffu};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
+    }
+  }
+  const int e = (int)(mx >> 7) - 127;  // exponent of the largest magnitude
+  const bool zero = mx == 0 || e > 127 - 14;
+  const float up = zero ? 1.0f : __uint_as_float((uint32_t)(127 + 14 - e) << 23);
+#pragma unroll 1
+  for (int c = 0; c < 8; c += 2) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      v[i] = valid ? __ldg(src + crank * 32 + c * 4 + i) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = v[4 * cc + i];
+        w[4 * i] = bf16x2_to_f16x2_mul(u.x, up);
+        w[4 * i + 1] = bf16x2_to_f16x2_mul(u.y, up);
+        w[4 * i + 2] = bf16x2_to_f16x2_mul(u.z, up);
+        w[4 * i + 3] = bf16x2_to_f16x2_mul(u.w, up);
+      }
+      tmem_st16(taddr + 16 * (c + cc), w);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 v = valid ? __ldg(src + 64 + crank * 4 + i) : make_uint4(0u, 0u, 0u, 0u);
+    v = make_uint4(bf16x2_to_f16x2_mul(v.x, up), bf16x2_to_f16x2_mul(v.y, up),
+                   bf16x2_to_f16x2_mul(v.z, up), bf16x2_to_f16x2_mul(v.w, up));
+    *reinterpret_cast<uint4*>(qr + ((i ^ (hrow & 7)) << 4)) = v;
+  }
+  tmem_st_wait();
+  return zero ? 1.0f : __uint_as_float((uint32_t)(127 - 14 + e) << 23);
+}
+
 template <int KVT, bool FUSED, bool SPARSE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_lat,
@@ -732,62 +786,25 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     float* xin = reinterpret_cast<float*>(smem + L::OFF_X);
     float* xself = reinterpret_cast<float*>(smem + L::OFF_SELF);
-    // Q of row r as FP16: this CTA's 256 latent dims into TMEM (two per column), its 32 RoPE
-    // dims into row h of the SW128 A-operand tile in shared memory.  The head's values are
-    // multiplied by 2^(14 - e), e the exponent of their largest magnitude (exact; keeps them
-    // in FP16's range), and the head's logits by qs = 2^(e - 14) to undo it.
-    float qs = 1.0f;
-    // Q of row r; the next row's Q is prefetched into L2, so that its load, which that row's
-    // first Q.K^T waits for, does not wait for DRAM.
+    float qs = 1.0f;  // 2^(e - 14) of this head's Q in the current row (see tc_load_q)
     auto load_q = [&](int64_t r) {
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) + (r * H + h) * kDqk);
-      if (h < H && r + 1 < p.rows) {
-        const char* qn = reinterpret_cast<const char*>(p.q) + ((r + 1) * H + h) * (kDqk * 2);
-#pragma unroll
-        for (int l = 0; l < 4; ++l) prefetch_l2(qn + crank * 512 + 128 * l);
-        prefetch_l2(qn + 1024);  // the RoPE dims of both CTAs
-      }
-      uint32_t mx = 0;  // largest |bf16| bit pattern over this CTA's 288 dims
-      if (h < H) {
-#pragma unroll 12
-        for (int i = 0; i < 36; ++i) {
-          const uint4 v = __ldg(src + (i < 32 ? crank * 32 + i : 64 + crank * 4 + (i - 32)));
-          const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
-                                 v.w & 0x7fff7fffu};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
-        }
-      }
-      const int e = (int)(mx >> 7) - 127;  // exponent of the largest magnitude
-      const bool zero = mx == 0 || e > 127 - 14;
-      const float up = zero ? 1.0f : __uint_as_float((uint32_t)(127 + 14 - e) << 23);
-      qs = zero ? 1.0f : __uint_as_float((uint32_t)(127 - 14 + e) << 23);
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (h < H) v = __ldg(src + crank * 32 + c * 4 + i);
-          w[4 * i] = bf16x2_to_f16x2_mul(v.x, up); w[4 * i + 1] = bf16x2_to_f16x2_mul(v.y, up);
-          w[4 * i + 2] = bf16x2_to_f16x2_mul(v.z, up); w[4 * i + 3] = bf16x2_to_f16x2_mul(v.w, up);
-        }
-        tmem_st16(trow + kColQ + 16 * c, w);
-      }
       unsigned char* qr = smem + L::OFF_QR + (h >> 3) * 1024 + (h & 7) * 128;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (h < H) v = __ldg(src + 64 + crank * 4 + i);
-        v = make_uint4(bf16x2_to_f16x2_mul(v.x, up), bf16x2_to_f16x2_mul(v.y, up),
-                       bf16x2_to_f16x2_mul(v.z, up), bf16x2_to_f16x2_mul(v.w, up));
-        *reinterpret_cast<uint4*>(qr + ((i ^ (h & 7)) << 4)) = v;
-      }
+      qs = tc_load_q(src, h < H, (int)crank, trow + kColQ, qr, h);
       fence_proxy_async_smem();
-      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.q_ready);
+    };
+    // this thread's lines of row r of Q into L2 (its CTA's latent half and the RoPE dims of
+    // both CTAs), a few tiles before the row is needed
+    auto prefetch_q = [&](int64_t r) {
+      if (h >= H || r >= p.rows) return;
+      const char* qn = reinterpret_cast<const char*>(p.q) + (r * H + h) * (kDqk * 2);
+#pragma unroll
+      for (int l = 0; l < 4; ++l) prefetch_l2(qn + crank * 512 + 128 * l);
+      prefetch_l2(qn + 1024);
     };
 
     Walk<FUSED, SPARSE> wa;
@@ -796,6 +813,9 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     if (ntiles > 0) load_q(wa.info.r);
     for (int j = 0; j < ntiles; ++j) {
       const int buf = j & 1;
+      // the next row's Q into L2 four tiles before this unit's end (the rows of the
+      // partial form's units follow one another too)
+      if (wa.lt == max(0, wa.info.ntile - 4)) prefetch_q(wa.info.r + 1);
       if (!mbar_wait(&sh.s_full[buf], (j >> 1) & 1, abort_flag)) break;
       if (!mbar_wait(&sh.kt_full[j % NK], (j / NK) & 1, abort_flag)) break;
       tc_fence_after();
