@@ -12,7 +12,7 @@
 // top 11 bits) is resolved by a histogram (shared-memory atomics) built while a list of up
 // to kTkStageMax entries is loaded and staged in shared memory; the bin that holds the k-th
 // largest key then usually holds a few hundred staged entries, whose 16-bit indices become
-// the candidates, and the remaining digits (10 bits each) look at the candidates only.  The
+// the candidates, and the remaining digits (9 bits each) look at the candidates only.  The
 // search stops as soon as a digit's bin is taken whole.  Lists longer than the staging, or
 // with more candidates than the buffer holds, resolve the further digits (11, 10, then the
 // low word) over every entry, re-reading global memory (L2) when not staged.  The
@@ -31,8 +31,9 @@ constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkBins = 2048;
 // candidates (the staged entries in the first digit's bin): their histogram takes the first
-// kTkCandBins words of the first digit's, their 16-bit staging indices the rest
-constexpr int kTkCandBins = 1024;
+// kTkCandBins words of the first digit's, their 16-bit staging indices the rest (3072; a
+// merge of lists that are each a shard's best entries puts ~13% of them in the first bin)
+constexpr int kTkCandBins = 512;
 constexpr int kTkCandCap = (kTkBins - kTkCandBins) * 2;
 constexpr int kTkRound = 4 * kTkThreads;  // entries per round: four consecutive per thread
 constexpr int kTkLoadRounds = 4;          // rounds whose loads are issued together
@@ -318,11 +319,11 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
     if (nc <= (uint32_t)kTkCandCap) {
       uint16_t* cand = reinterpret_cast<uint16_t*>(hist + kTkCandBins);
       for (uint32_t m = cmask; m != 0u; m &= m - 1u) cand[o++] = (uint16_t)(e0 + __ffs(m) - 1);
-      // digits of 10 bits (the last of each word narrower) over the candidates only
+      // digits of 9 bits (the last of each word narrower) over the candidates only
       for (int dg = 0; dg < 7 && !done; ++dg) {
         const bool lo = dg >= 3;
-        const int shift = dg == 0 ? 11 : dg == 1 ? 1 : dg == 2 ? 0 : dg == 3 ? 22 : dg == 4 ? 12 : dg == 5 ? 2 : 0;
-        const uint32_t wm = dg == 2 ? 1u : dg == 6 ? 3u : 1023u;
+        const int shift = dg == 0 ? 12 : dg == 1 ? 3 : dg == 2 ? 0 : dg == 3 ? 23 : dg == 4 ? 14 : dg == 5 ? 5 : 0;
+        const uint32_t wm = dg == 2 ? 7u : dg == 6 ? 31u : 511u;
         for (int i = tid; i < kTkCandBins; i += kTkThreads) hist[i] = 0u;
         __syncthreads();  // (also orders the candidate writes before their reads)
         for (int j = tid; j < (int)nc; j += kTkThreads) {
