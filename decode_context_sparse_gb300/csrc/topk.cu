@@ -196,6 +196,80 @@ __device__ __forceinline__ uint32_t tk_find_bin(const uint32_t* hist, uint32_t k
   return tot;
 }
 
+// The same search by one warp over NB bins (NB / 32 a multiple of 4, at most 64 bins a
+// lane), for the histograms that the whole block built: lane l sums the l-th group of
+// NB / 32 bins from the top (16-B reads in a lane-rotated order, so that the lanes of a
+// quarter warp hit distinct banks), a scan of the sums finds the group holding the krem-th
+// key, and a second scan over that group's bins (one or two a lane) the bin.  Every lane
+// returns the bin, *above and *binh; krem above the total gives bin 0 with nothing in it.
+template <int NB>
+__device__ __forceinline__ uint32_t tk_find_bin_warp(const uint32_t* hist, uint32_t krem,
+                                                     uint32_t* above, uint32_t* binh) {
+  constexpr int BPL = NB / 32;
+  static_assert(BPL % 4 == 0 && BPL <= 64, "whole 16-B pieces, at most two bins a lane after");
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const uint4* g = reinterpret_cast<const uint4*>(hist + NB - BPL * (lane + 1));
+  uint32_t s = 0;
+#pragma unroll
+  for (int q = 0; q < BPL / 4; ++q) {
+    const uint4 v = g[(q + lane) % (BPL / 4)];
+    s += (v.x + v.y) + (v.z + v.w);
+  }
+  uint32_t x = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kAll, x, o);
+    if (lane >= o) x += y;
+  }
+  const uint32_t hit = __ballot_sync(kAll, x >= krem);
+  if (hit == 0u) {
+    *above = __shfl_sync(kAll, x, 31);
+    *binh = 0u;
+    return 0u;
+  }
+  const int L = __ffs(hit) - 1;
+  const uint32_t cum = __shfl_sync(kAll, x - s, L);  // keys in the groups above group L
+  const int topL = NB - 1 - BPL * L;                  // group L's top bin
+  constexpr int PER = BPL >= 32 ? BPL / 32 : 1;       // bins a lane takes in group L
+  uint32_t h0 = 0u, h1 = 0u;
+  if (PER == 2) {
+    h0 = hist[topL - 2 * lane];
+    h1 = hist[topL - 2 * lane - 1];
+  } else if (lane < BPL) {
+    h0 = hist[topL - lane];
+  }
+  const uint32_t ps = h0 + h1;
+  uint32_t xx = ps;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kAll, xx, o);
+    if (lane >= o) xx += y;
+  }
+  const int J = __ffs(__ballot_sync(kAll, cum + xx >= krem)) - 1;  // (there is one)
+  const uint32_t before = cum + __shfl_sync(kAll, xx - ps, J);
+  const uint32_t a0 = __shfl_sync(kAll, h0, J), a1 = __shfl_sync(kAll, h1, J);
+  const bool first = PER == 1 || before + a0 >= krem;
+  *above = first ? before : before + a0;
+  *binh = first ? a0 : a1;
+  return (uint32_t)(PER == 2 ? topL - 2 * J - (first ? 0 : 1) : topL - J);
+}
+
+// tk_find_bin_warp by warp 0, its result in sh.bin, sh.above, sh.binh for every thread.
+template <int NB>
+__device__ __forceinline__ void tk_find_bin_w0(const uint32_t* hist, uint32_t krem, TkShared& sh) {
+  if (threadIdx.x < 32) {
+    uint32_t ab, bh;
+    const uint32_t b = tk_find_bin_warp<NB>(hist, krem, &ab, &bh);
+    if (threadIdx.x == 0) {
+      sh.bin = b;
+      sh.above = ab;
+      sh.binh = bh;
+    }
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t h, uint32_t msk, uint32_t pre,
                                          int shift, int nb) {
   // (msk covers the first digit and pre's first digit is a bin >= 1: h == 0 never counts)
@@ -275,7 +349,7 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
   }
   __syncthreads();
   // the first digit's bin; the valid entries are those outside bin 0
-  tk_find_bin<kTkBins / kTkThreads>(hist, (uint32_t)p.k, sh);
+  tk_find_bin_w0<kTkBins>(hist, (uint32_t)p.k, sh);
   const uint32_t nvalid = (uint32_t)(rounds * kTkRound) - hist[0];
   // more valid entries than k: a radix search for the k-th largest key T, the selection
   // being key >= T; else every valid entry (key >= 1)
@@ -337,7 +411,7 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
           }
         }
         __syncthreads();
-        tk_find_bin<kTkCandBins / kTkThreads>(hist, krem, sh);
+        tk_find_bin_w0<kTkCandBins>(hist, krem, sh);
         krem -= sh.above;
         if (!lo) {
           pre_hi |= sh.bin << shift;
@@ -347,7 +421,8 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
           msk_lo |= wm << shift;
         }
         done = sh.binh == krem;  // (always by the last digit: keys differ)
-        __syncthreads();  // every thread has read the bin before the histogram is cleared
+        // (the next digit's clear follows its reads of sh and of the histogram: warp 0 read
+        // the histogram before the barrier above, and sh is next written after two more)
       }
     } else {
       wide = true;
