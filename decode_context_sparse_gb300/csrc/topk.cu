@@ -270,6 +270,14 @@ __device__ __forceinline__ void tk_find_bin_w0(const uint32_t* hist, uint32_t kr
   __syncthreads();
 }
 
+// A 16-B asynchronous copy from global to shared memory (both 16-B aligned), and the wait
+// for every such copy of the calling thread.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t h, uint32_t msk, uint32_t pre,
                                          int shift, int nb) {
   // (msk covers the first digit and pre's first digit is a bin >= 1: h == 0 never counts)
@@ -319,9 +327,41 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
 
   // pass 0: stage the keys and build the histogram of the first digit.  Every entry counts,
   // the invalid ones (key 0, and the entries past the end) in bin 0, which holds no valid key.
+  // Staged aligned candidate lists: every round's scores are copied into the staging at once
+  // (asynchronous 16-B copies, no registers held), then turned into keys in place; a thread
+  // reads back only the pieces it copied.
+  const bool async = !MERGE && staged && src.vec;
+  if (async) {
+#pragma unroll
+    for (int c = 0; c < kTkBlockRounds; ++c) {
+      const int i = c * kTkRound + 4 * tid;
+      if (c < rounds && i + 3 < n) cp_async16(keys + i, src.sc + i);
+    }
+  }
   for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
   __syncthreads();
-  for (int c0 = 0; c0 < rounds; c0 += kTkLoadRounds) {
+  if (async) {
+    cp_async_wait_all();
+#pragma unroll
+    for (int c = 0; c < kTkBlockRounds; ++c) {
+      if (c < rounds) {
+        const int i = c * kTkRound + 4 * tid;
+        float4 v;
+        int4 t;
+        if (i + 3 < n)
+          v = *reinterpret_cast<const float4*>(keys + i);
+        else
+          src.raw4(i, v, t);  // the ragged end, from global memory
+        const uint4 k4 = src.keys_of(v, t);
+        *reinterpret_cast<uint4*>(keys + i) = k4;
+        atomicAdd(&hist[k4.x >> 21], 1u);
+        atomicAdd(&hist[k4.y >> 21], 1u);
+        atomicAdd(&hist[k4.z >> 21], 1u);
+        atomicAdd(&hist[k4.w >> 21], 1u);
+      }
+    }
+  }
+  for (int c0 = 0; c0 < (async ? 0 : rounds); c0 += kTkLoadRounds) {
     // every load of kTkLoadRounds rounds in flight before any is used
     float4 v[kTkLoadRounds];
     int4 t[kTkLoadRounds];
@@ -366,24 +406,28 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
   const int e0 = 32 * tid, lim = rounds * kTkRound;
   uint32_t amask = 0u, cmask = 0u;
   if (staged) {
+    // above the bin: key > thr_a (no key when b0 is the top bin); in or above it: key >= thr_c.
+    // Chunk j's bits go to positions 4j..4j+3 and the masks are rotated into entry order
+    // at the end (chunk j holds entries 4 ((j + tid) mod 8) ..).
+    const uint32_t thr_a = (uint32_t)((((uint64_t)b0 + 1u) << 21) - 1u);
+    const uint32_t thr_c = b0 << 21;
+    uint32_t ar = 0u, cr = 0u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int jj = (j + tid) & 7;
-      const int i = e0 + 4 * jj;
+      const int i = e0 + 4 * ((j + tid) & 7);
       if (i < lim) {  // (entries past the staged rounds are past the end)
         const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
-        const uint32_t d[4] = {k4.x >> 21, k4.y >> 21, k4.z >> 21, k4.w >> 21};
-        uint32_t a4 = 0u, c4 = 0u;
+        const uint32_t k[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          a4 |= (uint32_t)(d[e] > b0) << e;
-          c4 |= (uint32_t)(d[e] == b0) << e;
+          if (k[e] > thr_a) ar |= 1u << (4 * j + e);
+          if (k[e] >= thr_c) cr |= 1u << (4 * j + e);
         }
-        amask |= a4 << (4 * jj);
-        cmask |= c4 << (4 * jj);
       }
     }
-    if (!search) cmask = 0u;  // (bin 0: the invalid entries)
+    const int rot = 4 * (tid & 7);
+    amask = __funnelshift_l(ar, ar, rot);
+    cmask = search ? __funnelshift_l(cr, cr, rot) & ~amask : 0u;  // (bin 0: the invalid entries)
   }
   bool wide = !staged;  // the further digits run over every entry
   if (!done && staged) {
