@@ -299,6 +299,20 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t li = blockIdx.x;
 
+  // aligned candidate lists whose whole row stride fits the staging: every 16-B piece of
+  // the row is copied into the staging at once (asynchronous copies, no registers held),
+  // before the list's length is known; the pieces are turned into keys in place below, each
+  // by the thread that copied it
+  const bool async = !MERGE && p.vec && p.stride <= p.stage;
+  if (async) {
+    const float* row = p.score + li * (int64_t)p.stride;
+#pragma unroll
+    for (int c = 0; c < kTkBlockRounds; ++c) {
+      const int i = c * kTkRound + 4 * tid;
+      if (i < p.stride) cp_async16(keys + i, row + i);
+    }
+  }
+
   TkList<MERGE> src;
   src.vec = p.vec != 0;
   src.div = p.div;
@@ -327,17 +341,6 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
 
   // pass 0: stage the keys and build the histogram of the first digit.  Every entry counts,
   // the invalid ones (key 0, and the entries past the end) in bin 0, which holds no valid key.
-  // Staged aligned candidate lists: every round's scores are copied into the staging at once
-  // (asynchronous 16-B copies, no registers held), then turned into keys in place; a thread
-  // reads back only the pieces it copied.
-  const bool async = !MERGE && staged && src.vec;
-  if (async) {
-#pragma unroll
-    for (int c = 0; c < kTkBlockRounds; ++c) {
-      const int i = c * kTkRound + 4 * tid;
-      if (c < rounds && i + 3 < n) cp_async16(keys + i, src.sc + i);
-    }
-  }
   for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
   __syncthreads();
   if (async) {
@@ -346,12 +349,14 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
     for (int c = 0; c < kTkBlockRounds; ++c) {
       if (c < rounds) {
         const int i = c * kTkRound + 4 * tid;
-        float4 v;
+        float4 v = *reinterpret_cast<const float4*>(keys + i);
+        if (i + 3 >= n) {  // the ragged end: entries past the list count as -inf
+          v.x = i < n ? v.x : -INFINITY;
+          v.y = i + 1 < n ? v.y : -INFINITY;
+          v.z = i + 2 < n ? v.z : -INFINITY;
+          v.w = i + 3 < n ? v.w : -INFINITY;
+        }
         int4 t;
-        if (i + 3 < n)
-          v = *reinterpret_cast<const float4*>(keys + i);
-        else
-          src.raw4(i, v, t);  // the ragged end, from global memory
         const uint4 k4 = src.keys_of(v, t);
         *reinterpret_cast<uint4*>(keys + i) = k4;
         atomicAdd(&hist[k4.x >> 21], 1u);
