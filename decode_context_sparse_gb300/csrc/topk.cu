@@ -278,6 +278,68 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// The first digit's bin (kTkBins = 128 bins per warp): warp w sums bins [128 w, 128 w + 128)
+// (one 16-B read a lane), then warp 0 finds the group holding the krem-th key counting from
+// the top and the bin within it (a 16-B read a lane again).  Results in sh as tk_find_bin.
+__device__ __forceinline__ void tk_find_bin_first(const uint32_t* hist, uint32_t krem, TkShared& sh) {
+  static_assert(kTkBins == 128 * kTkWarps, "a group of 128 bins per warp");
+  constexpr unsigned kAll = 0xffffffffu;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  {
+    const uint4 v = reinterpret_cast<const uint4*>(hist + 128 * warp)[lane];
+    const uint32_t g = __reduce_add_sync(kAll, (v.x + v.y) + (v.z + v.w));
+    if (lane == 0) sh.ws[warp] = g;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t s = lane < kTkWarps ? sh.ws[kTkWarps - 1 - lane] : 0u;  // groups from the top
+    uint32_t x = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kAll, x, o);
+      if (lane >= o) x += y;
+    }
+    const uint32_t hit = __ballot_sync(kAll, lane < kTkWarps && x >= krem);
+    uint32_t bin = 0u, above = __shfl_sync(kAll, x, 31), binh = 0u;
+    if (hit != 0u) {
+      const int gl = __ffs(hit) - 1;
+      const int grp = kTkWarps - 1 - gl;
+      const uint32_t cum = __shfl_sync(kAll, x - s, gl);
+      // lane j: the group's bins 4 (31 - j) .. 4 (31 - j) + 3, from the top
+      const uint4 q = reinterpret_cast<const uint4*>(hist + 128 * grp)[31 - lane];
+      const uint32_t ps = (q.x + q.y) + (q.z + q.w);
+      uint32_t xx = ps;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kAll, xx, o);
+        if (lane >= o) xx += y;
+      }
+      const int J = __ffs(__ballot_sync(kAll, cum + xx >= krem)) - 1;  // (there is one)
+      uint32_t before = cum + __shfl_sync(kAll, xx - ps, J);
+      const uint32_t a[4] = {__shfl_sync(kAll, q.w, J), __shfl_sync(kAll, q.z, J),
+                             __shfl_sync(kAll, q.y, J), __shfl_sync(kAll, q.x, J)};
+      const int base = 128 * grp + 4 * (31 - J) + 3;
+      bool found = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (!found && before + a[e] >= krem) {
+          found = true;
+          bin = (uint32_t)(base - e);
+          above = before;
+          binh = a[e];
+        }
+        if (!found) before += a[e];
+      }
+    }
+    if (lane == 0) {
+      sh.bin = bin;
+      sh.above = above;
+      sh.binh = binh;
+    }
+  }
+  __syncthreads();
+}
+
 __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t h, uint32_t msk, uint32_t pre,
                                          int shift, int nb) {
   // (msk covers the first digit and pre's first digit is a bin >= 1: h == 0 never counts)
@@ -394,7 +456,7 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
   }
   __syncthreads();
   // the first digit's bin; the valid entries are those outside bin 0
-  tk_find_bin_w0<kTkBins>(hist, (uint32_t)p.k, sh);
+  tk_find_bin_first(hist, (uint32_t)p.k, sh);
   const uint32_t nvalid = (uint32_t)(rounds * kTkRound) - hist[0];
   // more valid entries than k: a radix search for the k-th largest key T, the selection
   // being key >= T; else every valid entry (key >= 1)
@@ -669,10 +731,19 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
     if (tid == 0) sh.maxid = -1;
     __syncthreads();
     int mx = -1;
-    for (int j = tid; j < cnt; j += kTkThreads) {
-      const int id = src.gid(sorted[j]);
-      sorted[j] = id;
-      mx = max(mx, id);
+    for (int j0 = tid; j0 < cnt; j0 += 4 * kTkThreads) {  // four id loads in flight
+      int id[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kTkThreads;
+        id[u] = j < cnt ? src.gid(sorted[j]) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u * kTkThreads;
+        if (j < cnt) sorted[j] = id[u];
+        mx = max(mx, id[u]);
+      }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0 && mx >= 0) atomicMax(&sh.maxid, mx);
