@@ -170,6 +170,30 @@ def test_local_then_merge_is_the_unsharded_topk(dcp, D, I, k):
     assert np.array_equal(top.cpu().numpy(), wt) and np.array_equal(cnt.cpu().numpy(), wc)
 
 
+def test_infinities_and_signed_zeros(dcp):
+    """+inf ranks above every finite score, -inf and NaN are never candidates, -0 ranks as
+    +0 (ties by slot), through both kernels; aligned rows of 6000 and unaligned ones of
+    1001 take the two staging paths."""
+    for stride in (6000, 1001):
+        D, R, k = 4, 4, 700
+        rng = np.random.default_rng(stride)
+        sc = rng.standard_normal((D, R, stride)).astype(np.float32)
+        u = rng.random(sc.shape)
+        sc[u < 0.01] = np.inf
+        sc[(u >= 0.01) & (u < 0.02)] = -np.inf
+        sc[(u >= 0.02) & (u < 0.03)] = np.nan
+        sc[(u >= 0.03) & (u < 0.06)] = 0.0
+        sc[(u >= 0.06) & (u < 0.09)] = -0.0
+        sc[:, 3, :] = np.where(rng.random((D, stride)) < 0.5, np.float32(-0.0), np.float32(0.0))
+        ll = np.full((D, R), stride, dtype=np.int32)
+        ll[:, 1] = stride - 3
+        cs, ci = _check_local(dcp, torch.from_numpy(sc), ll, k, D, 1)
+        top, cnt = dcp.dcp_topk_merge(cs, ci, k)
+        torch.cuda.synchronize()
+        wt, wc = otk.merge_topk(cs.cpu().numpy(), ci.cpu().numpy(), k)
+        assert np.array_equal(top.cpu().numpy(), wt) and np.array_equal(cnt.cpu().numpy(), wc)
+
+
 def test_full_size_topk2048_batch(dcp):
     """The top-k 2048 decode batch: 8 shards x 384 rows x 16384 local slots, k = 2048, in the
     launch configuration the bench times.  Every row's global top-k is compared with the
