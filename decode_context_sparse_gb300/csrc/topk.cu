@@ -10,9 +10,11 @@
 // selected; -0 maps like +0); the low word is the complement of the global slot id, so a
 // larger key ranks first and the keys of one list are distinct.  The first digit (the
 // top 11 bits) is resolved by a histogram (shared-memory atomics) built while a list of up
-// to kTkStageMax entries is loaded and staged in shared memory; the bin that holds the k-th
-// largest key then usually holds a few hundred staged entries, whose 16-bit indices become
-// the candidates, and the remaining digits (9 bits each) look at the candidates only.  The
+// to kTkStageMax entries is staged in shared memory (aligned candidate lists: every 16-B
+// piece of the row copied asynchronously at once, then turned into keys in place; otherwise
+// through registers); the bin that holds the k-th largest key then usually holds a few
+// hundred staged entries, whose 16-bit indices become the candidates, and the remaining
+// digits (9 bits each) look at the candidates only, each digit's bin found by one warp.  The
 // search stops as soon as a digit's bin is taken whole.  Lists longer than the staging, or
 // with more candidates than the buffer holds, resolve the further digits (11, 10, then the
 // low word) over every entry, re-reading global memory (L2) when not staged.  The
