@@ -967,7 +967,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       };
 #pragma unroll 1
       for (int rc = 0; rc < 4; ++rc) {
-        const int c0 = half * 8 + 2 * rc;  // first 16-column chunk of this round
+        const int c0 = half * 8 + 2 * rc;  // first 16-column chunk of pass rc
         uint32_t v[2][16];
         tmem_ld16(trow + kColO + 16 * c0, v[0]);
         tmem_ld16(trow + kColO + 16 * (c0 + 1), v[1]);
