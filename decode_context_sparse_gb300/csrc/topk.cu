@@ -403,474 +403,496 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
     return staged ? *reinterpret_cast<const uint4*>(keys + i) : src.key4(i);
   };
 
-  // pass 0: stage the keys and build the histogram of the first digit.  Every entry counts,
-  // the invalid ones (key 0, and the entries past the end) in bin 0, which holds no valid key.
-  for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
-  __syncthreads();
-  if (async) {
-    cp_async_wait_all();
+  // A merge first selects by score alone (the ids not read): the result is the same unless
+  // an entry with a padding id (< 0) is selected, which the id pass after the compaction
+  // sees; the merge then selects again with the ids.  (A padding entry below the threshold
+  // cannot move it; in a tie at the threshold the padding ids rank last.)
+  for (int attempt = 0;; ++attempt) {
+    const bool exact = !MERGE || attempt > 0;
+    const bool masync = MERGE && !exact && staged && src.vec;
+    if (masync) {  // the scores, every piece at once (n is a multiple of 4)
 #pragma unroll
-    for (int c = 0; c < kTkBlockRounds; ++c) {
-      if (c < rounds) {
+      for (int c = 0; c < kTkBlockRounds; ++c) {
         const int i = c * kTkRound + 4 * tid;
-        float4 v = *reinterpret_cast<const float4*>(keys + i);
-        if (i + 3 >= n) {  // the ragged end: entries past the list count as -inf
-          v.x = i < n ? v.x : -INFINITY;
-          v.y = i + 1 < n ? v.y : -INFINITY;
-          v.z = i + 2 < n ? v.z : -INFINITY;
-          v.w = i + 3 < n ? v.w : -INFINITY;
-        }
-        int4 t;
-        const uint4 k4 = src.keys_of(v, t);
-        *reinterpret_cast<uint4*>(keys + i) = k4;
-        atomicAdd(&hist[k4.x >> 21], 1u);
-        atomicAdd(&hist[k4.y >> 21], 1u);
-        atomicAdd(&hist[k4.z >> 21], 1u);
-        atomicAdd(&hist[k4.w >> 21], 1u);
+        if (i < n) cp_async16(keys + i, src.sc + src.off(i));
       }
     }
-  }
-  for (int c0 = 0; c0 < (async ? 0 : rounds); c0 += kTkLoadRounds) {
-    // every load of kTkLoadRounds rounds in flight before any is used
-    float4 v[kTkLoadRounds];
-    int4 t[kTkLoadRounds];
-#pragma unroll
-    for (int u = 0; u < kTkLoadRounds; ++u) {
-      if (c0 + u < rounds) {
-        src.raw4((c0 + u) * kTkRound + 4 * tid, v[u], t[u]);
-      } else {
-        v[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        t[u] = make_int4(-1, -1, -1, -1);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kTkLoadRounds; ++u) {
-      if (c0 + u < rounds) {
-        const uint4 k4 = src.keys_of(v[u], t[u]);
-        if (staged)  // the staging is a whole number of rounds
-          *reinterpret_cast<uint4*>(keys + (c0 + u) * kTkRound + 4 * tid) = k4;
-        atomicAdd(&hist[k4.x >> 21], 1u);
-        atomicAdd(&hist[k4.y >> 21], 1u);
-        atomicAdd(&hist[k4.z >> 21], 1u);
-        atomicAdd(&hist[k4.w >> 21], 1u);
-      }
-    }
-  }
-  __syncthreads();
-  // the first digit's bin; the valid entries are those outside bin 0
-  tk_find_bin_first(hist, (uint32_t)p.k, sh);
-  const uint32_t nvalid = (uint32_t)(rounds * kTkRound) - hist[0];
-  // more valid entries than k: a radix search for the k-th largest key T, the selection
-  // being key >= T; else every valid entry (key >= 1)
-  const bool search = nvalid > (uint32_t)p.k;
-  const uint32_t b0 = search ? sh.bin : 0u;
-  uint32_t krem = search ? (uint32_t)p.k - sh.above : 0u;
-  bool done = !search || sh.binh == krem;  // (a bin taken whole ends the search)
-  uint32_t pre_hi = search ? b0 << 21 : 1u, msk_hi = 0xffe00000u, pre_lo = 0, msk_lo = 0;
 
-  // staged lists: one pass over this thread's run of 32 entries [32 tid, 32 tid + 32) (read
-  // in a rotated chunk order, so that the threads of a warp hit distinct banks) sorts them
-  // into those above the first digit's bin (selected whatever T is) and those in it (the
-  // candidates); bit b of a mask is entry 32 tid + b
-  const int e0 = 32 * tid, lim = rounds * kTkRound;
-  uint32_t amask = 0u, cmask = 0u;
-  if (staged) {
-    // above the bin: key > thr_a (no key when b0 is the top bin); in or above it: key >= thr_c.
-    // Chunk j's bits go to positions 4j..4j+3 and the masks are rotated into entry order
-    // at the end (chunk j holds entries 4 ((j + tid) mod 8) ..).
-    const uint32_t thr_a = (uint32_t)((((uint64_t)b0 + 1u) << 21) - 1u);
-    const uint32_t thr_c = b0 << 21;
-    uint32_t ar = 0u, cr = 0u;
+    // pass 0: stage the keys and build the histogram of the first digit.  Every entry counts,
+    // the invalid ones (key 0, and the entries past the end) in bin 0, which holds no valid key.
+    for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
+    __syncthreads();
+    if (async || masync) {
+      cp_async_wait_all();
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = e0 + 4 * ((j + tid) & 7);
-      if (i < lim) {  // (entries past the staged rounds are past the end)
-        const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
-        const uint32_t k[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (k[e] > thr_a) ar |= 1u << (4 * j + e);
-          if (k[e] >= thr_c) cr |= 1u << (4 * j + e);
-        }
-      }
-    }
-    const int rot = 4 * (tid & 7);
-    amask = __funnelshift_l(ar, ar, rot);
-    cmask = search ? __funnelshift_l(cr, cr, rot) & ~amask : 0u;  // (bin 0: the invalid entries)
-  }
-  bool wide = !staged;  // the further digits run over every entry
-  if (!done && staged) {
-    // the candidates' 16-bit staging indices go to the histogram's upper words
-    uint32_t nc;
-    uint32_t o = tk_scan((uint32_t)__popc(cmask), sh.ws, &nc);  // (after every read of hist)
-    if (nc <= (uint32_t)kTkCandCap) {
-      uint16_t* cand = reinterpret_cast<uint16_t*>(hist + kTkCandBins);
-      for (uint32_t m = cmask; m != 0u; m &= m - 1u) cand[o++] = (uint16_t)(e0 + __ffs(m) - 1);
-      // digits of 9 bits (the last of each word narrower) over the candidates only
-      for (int dg = 0; dg < 7 && !done; ++dg) {
-        const bool lo = dg >= 3;
-        const int shift = dg == 0 ? 12 : dg == 1 ? 3 : dg == 2 ? 0 : dg == 3 ? 23 : dg == 4 ? 14 : dg == 5 ? 5 : 0;
-        const uint32_t wm = dg == 2 ? 7u : dg == 6 ? 31u : 511u;
-        for (int i = tid; i < kTkCandBins; i += kTkThreads) hist[i] = 0u;
-        __syncthreads();  // (also orders the candidate writes before their reads)
-        for (int j = tid; j < (int)nc; j += kTkThreads) {
-          const int i = cand[j];
-          const uint32_t h = keys[i];
-          if (!lo) {
-            if ((h & msk_hi) == pre_hi) atomicAdd(&hist[(h >> shift) & wm], 1u);
-          } else if (h == pre_hi) {
-            const uint32_t l = ~(uint32_t)src.gid(i);
-            if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & wm], 1u);
+      for (int c = 0; c < kTkBlockRounds; ++c) {
+        if (c < rounds) {
+          const int i = c * kTkRound + 4 * tid;
+          float4 v = *reinterpret_cast<const float4*>(keys + i);
+          if (i + 3 >= n) {  // the ragged end: entries past the list count as -inf
+            v.x = i < n ? v.x : -INFINITY;
+            v.y = i + 1 < n ? v.y : -INFINITY;
+            v.z = i + 2 < n ? v.z : -INFINITY;
+            v.w = i + 3 < n ? v.w : -INFINITY;
           }
+          const int4 t = make_int4(0, 0, 0, 0);  // (a merge's first selection: ids not read)
+          const uint4 k4 = src.keys_of(v, t);
+          *reinterpret_cast<uint4*>(keys + i) = k4;
+          atomicAdd(&hist[k4.x >> 21], 1u);
+          atomicAdd(&hist[k4.y >> 21], 1u);
+          atomicAdd(&hist[k4.z >> 21], 1u);
+          atomicAdd(&hist[k4.w >> 21], 1u);
         }
-        __syncthreads();
-        tk_find_bin_w0<kTkCandBins>(hist, krem, sh);
-        krem -= sh.above;
-        if (!lo) {
-          pre_hi |= sh.bin << shift;
-          msk_hi |= wm << shift;
-        } else {
-          pre_lo |= sh.bin << shift;
-          msk_lo |= wm << shift;
-        }
-        done = sh.binh == krem;  // (always by the last digit: keys differ)
-        // (the next digit's clear follows its reads of sh and of the histogram: warp 0 read
-        // the histogram before the barrier above, and sh is next written after two more)
       }
-    } else {
-      wide = true;
     }
-  }
-  if (search) {
-    // the further digits over every entry: lists past the staging, or too many candidates
-    for (int dg = 1; dg < 6 && wide && !done; ++dg) {
-      const bool lo = dg >= 3;
-      const int shift = dg % 3 == 1 ? 10 : dg % 3 == 2 ? 0 : 21;
-      const int nb = dg % 3 == 2 ? 1024 : 2048;
-      for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
-      __syncthreads();
-      if (staged && !lo) {
-        // a high-word digit over the staged keys: compile-time shifts, one 16-B load per
-        // four keys, an atomic only for the keys still in play
-        for (int c = 0; c < rounds; ++c) {
-          const uint4 k4 = *reinterpret_cast<const uint4*>(keys + c * kTkRound + 4 * tid);
-          const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+    for (int c0 = 0; c0 < (async || masync ? 0 : rounds); c0 += kTkLoadRounds) {
+      // every load of kTkLoadRounds rounds in flight before any is used
+      float4 v[kTkLoadRounds];
+      int4 t[kTkLoadRounds];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if ((h[e] & msk_hi) == pre_hi)
-              atomicAdd(&hist[dg == 1 ? (h[e] >> 10) & 2047u : h[e] & 1023u], 1u);
+      for (int u = 0; u < kTkLoadRounds; ++u) {
+        if (c0 + u < rounds) {
+          src.raw4((c0 + u) * kTkRound + 4 * tid, v[u], t[u]);
+        } else {
+          v[u] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+          t[u] = make_int4(-1, -1, -1, -1);
         }
-      } else {
-        for (int c = 0; c < rounds; ++c) {
-          const uint4 k4 = get4(c);
-          const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+      }
+#pragma unroll
+      for (int u = 0; u < kTkLoadRounds; ++u) {
+        if (c0 + u < rounds) {
+          const uint4 k4 = src.keys_of(v[u], t[u]);
+          if (staged)  // the staging is a whole number of rounds
+            *reinterpret_cast<uint4*>(keys + (c0 + u) * kTkRound + 4 * tid) = k4;
+          atomicAdd(&hist[k4.x >> 21], 1u);
+          atomicAdd(&hist[k4.y >> 21], 1u);
+          atomicAdd(&hist[k4.z >> 21], 1u);
+          atomicAdd(&hist[k4.w >> 21], 1u);
+        }
+      }
+    }
+    __syncthreads();
+    // the first digit's bin; the valid entries are those outside bin 0
+    tk_find_bin_first(hist, (uint32_t)p.k, sh);
+    const uint32_t nvalid = (uint32_t)(rounds * kTkRound) - hist[0];
+    // more valid entries than k: a radix search for the k-th largest key T, the selection
+    // being key >= T; else every valid entry (key >= 1)
+    const bool search = nvalid > (uint32_t)p.k;
+    const uint32_t b0 = search ? sh.bin : 0u;
+    uint32_t krem = search ? (uint32_t)p.k - sh.above : 0u;
+    bool done = !search || sh.binh == krem;  // (a bin taken whole ends the search)
+    uint32_t pre_hi = search ? b0 << 21 : 1u, msk_hi = 0xffe00000u, pre_lo = 0, msk_lo = 0;
+
+    // staged lists: one pass over this thread's run of 32 entries [32 tid, 32 tid + 32) (read
+    // in a rotated chunk order, so that the threads of a warp hit distinct banks) sorts them
+    // into those above the first digit's bin (selected whatever T is) and those in it (the
+    // candidates); bit b of a mask is entry 32 tid + b
+    const int e0 = 32 * tid, lim = rounds * kTkRound;
+    uint32_t amask = 0u, cmask = 0u;
+    if (staged) {
+      // above the bin: key > thr_a (no key when b0 is the top bin); in or above it: key >= thr_c.
+      // Chunk j's bits go to positions 4j..4j+3 and the masks are rotated into entry order
+      // at the end (chunk j holds entries 4 ((j + tid) mod 8) ..).
+      const uint32_t thr_a = (uint32_t)((((uint64_t)b0 + 1u) << 21) - 1u);
+      const uint32_t thr_c = b0 << 21;
+      uint32_t ar = 0u, cr = 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = e0 + 4 * ((j + tid) & 7);
+        if (i < lim) {  // (entries past the staged rounds are past the end)
+          const uint4 k4 = *reinterpret_cast<const uint4*>(keys + i);
+          const uint32_t k[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
+            if (k[e] > thr_a) ar |= 1u << (4 * j + e);
+            if (k[e] >= thr_c) cr |= 1u << (4 * j + e);
+          }
+        }
+      }
+      const int rot = 4 * (tid & 7);
+      amask = __funnelshift_l(ar, ar, rot);
+      cmask = search ? __funnelshift_l(cr, cr, rot) & ~amask : 0u;  // (bin 0: the invalid entries)
+    }
+    bool wide = !staged;  // the further digits run over every entry
+    if (!done && staged) {
+      // the candidates' 16-bit staging indices go to the histogram's upper words
+      uint32_t nc;
+      uint32_t o = tk_scan((uint32_t)__popc(cmask), sh.ws, &nc);  // (after every read of hist)
+      if (nc <= (uint32_t)kTkCandCap) {
+        uint16_t* cand = reinterpret_cast<uint16_t*>(hist + kTkCandBins);
+        for (uint32_t m = cmask; m != 0u; m &= m - 1u) cand[o++] = (uint16_t)(e0 + __ffs(m) - 1);
+        // digits of 9 bits (the last of each word narrower) over the candidates only
+        for (int dg = 0; dg < 7 && !done; ++dg) {
+          const bool lo = dg >= 3;
+          const int shift = dg == 0 ? 12 : dg == 1 ? 3 : dg == 2 ? 0 : dg == 3 ? 23 : dg == 4 ? 14 : dg == 5 ? 5 : 0;
+          const uint32_t wm = dg == 2 ? 7u : dg == 6 ? 31u : 511u;
+          for (int i = tid; i < kTkCandBins; i += kTkThreads) hist[i] = 0u;
+          __syncthreads();  // (also orders the candidate writes before their reads)
+          for (int j = tid; j < (int)nc; j += kTkThreads) {
+            const int i = cand[j];
+            const uint32_t h = keys[i];
             if (!lo) {
-              hist_add(hist, h[e], msk_hi, pre_hi, shift, nb);
-            } else if (h[e] == pre_hi) {
-              const uint32_t l = ~(uint32_t)src.gid(c * kTkRound + 4 * tid + e);
-              if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
-            }
-          }
-        }
-      }
-      __syncthreads();
-      if (nb == 2048)
-        tk_find_bin<2048 / kTkThreads>(hist, krem, sh);
-      else
-        tk_find_bin<1024 / kTkThreads>(hist, krem, sh);
-      krem -= sh.above;
-      if (!lo) {
-        pre_hi |= sh.bin << shift;
-        msk_hi |= (uint32_t)(nb - 1) << shift;
-      } else {
-        pre_lo |= sh.bin << shift;
-        msk_lo |= (uint32_t)(nb - 1) << shift;
-      }
-      done = sh.binh == krem;
-      __syncthreads();  // every thread has read the bin before the histogram is cleared
-    }
-  }
-  const uint32_t t_hi = pre_hi, t_lo = pre_lo;
-
-  auto selected = [&](uint32_t h, int i) -> bool {
-    return h != 0u && (h > t_hi || (h == t_hi && (t_lo == 0u || ~(uint32_t)src.gid(i) >= t_lo)));
-  };
-  const bool no_ties = t_lo == 0u;  // then the selection is key >= t_hi (t_hi >= 1)
-  // write selected entry i (with key h) at output position pos (< k)
-  auto emit = [&](int i, uint32_t h, uint32_t pos) {
-    if (MERGE) {
-      sorted[pos] = i;  // the entry; its id is loaded below, all at once
-    } else {
-      // the score from its key (exact; a zero is re-read, the key merges -0 and +0)
-      p.cand_score[li * p.k + pos] = h == 0x80000000u ? src.score(i) : key_score(h);
-      p.cand_idx[li * p.k + pos] = src.gid(i);
-    }
-  };
-  if (staged) {
-    // the candidates that reach T join the entries above the first digit's bin; then a
-    // stable compaction: one block scan of the counts, each thread's entries in order
-    for (uint32_t m = cmask; m != 0u; m &= m - 1u) {
-      const int b = __ffs(m) - 1;
-      if (selected(keys[e0 + b], e0 + b)) amask |= 1u << b;
-    }
-    uint32_t smask = amask;
-    uint32_t total;
-    uint32_t pos = tk_scan((uint32_t)__popc(smask), sh.ws, &total);
-    // candidate lists with k <= kTkBins: the selected entries' indices go to the histogram's
-    // words first, and are written out with consecutive threads on consecutive positions
-    const bool via_smem = !MERGE && p.k <= kTkBins;
-    int32_t* sel = reinterpret_cast<int32_t*>(hist);
-    while (smask != 0u && pos < (uint32_t)p.k) {
-      const int e = __ffs(smask) - 1;
-      smask &= smask - 1u;
-      const int i = e0 + e;
-      if (via_smem)
-        sel[pos++] = i;
-      else
-        emit(i, keys[i], pos++);
-    }
-    if (tid == 0) sh.base = total;
-    __syncthreads();
-    if (via_smem) {
-      const int ns = (int)min(total, (uint32_t)p.k);
-      for (int j = tid; j < ns; j += kTkThreads) {
-        const int i = sel[j];
-        emit(i, keys[i], (uint32_t)j);
-      }
-    }
-  } else {
-    // lists past the staging: the keys come from L2, in rounds; a block of kTkBlockRounds
-    // rounds at a time: count per (round, warp), one scan, then each warp writes its entries
-    // at positions found with ballots
-    auto sel4 = [&](const uint4& k4, int i) -> uint32_t {  // bit e: entry i + e is selected
-      if (no_ties)
-        return (uint32_t)(k4.x >= t_hi) | (uint32_t)(k4.y >= t_hi) << 1 |
-               (uint32_t)(k4.z >= t_hi) << 2 | (uint32_t)(k4.w >= t_hi) << 3;
-      return (uint32_t)selected(k4.x, i) | (uint32_t)selected(k4.y, i + 1) << 1 |
-             (uint32_t)selected(k4.z, i + 2) << 2 | (uint32_t)selected(k4.w, i + 3) << 3;
-    };
-    if (tid == 0) sh.base = 0u;
-    for (int c0 = 0; c0 < rounds; c0 += kTkBlockRounds) {
-      const int nr = min(kTkBlockRounds, rounds - c0);
-      uint32_t selmask = 0;  // 4 bits per round of the block
-      for (int cr = 0; cr < nr; ++cr) {
-        const int c = c0 + cr;
-        const uint32_t m4 = sel4(get4(c), c * kTkRound + 4 * tid);
-        selmask |= m4 << (4 * cr);
-        const uint32_t wsum = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(m4));
-        if (lane == 0) sh.cw[cr][warp] = wsum;
-      }
-      __syncthreads();
-      if (warp == 0) {  // exclusive scan of the block's (round, warp) counts in index order
-        const int per = kTkBlockRounds * kTkWarps / 32;
-        uint32_t v[kTkBlockRounds * kTkWarps / 32], run = 0;
-#pragma unroll
-        for (int j = 0; j < per; ++j) {
-          const int q = lane * per + j;
-          v[j] = q / kTkWarps < nr ? sh.cw[q / kTkWarps][q % kTkWarps] : 0u;
-          run += v[j];
-        }
-        uint32_t x = run;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        uint32_t pos = sh.base + x - run;
-#pragma unroll
-        for (int j = 0; j < per; ++j) {
-          const int q = lane * per + j;
-          sh.off[q / kTkWarps][q % kTkWarps] = pos;
-          pos += v[j];
-        }
-        const uint32_t total = __shfl_sync(0xffffffffu, x, 31);
-        __syncwarp();
-        if (lane == 0) sh.base += total;
-      }
-      __syncthreads();
-      const uint32_t lt = (1u << lane) - 1u;
-      for (int cr = 0; cr < nr; ++cr) {
-        const int c = c0 + cr;
-        const uint32_t m4 = (selmask >> (4 * cr)) & 15u;
-        // entries of lower lanes come first, then this lane's in order
-        uint32_t pos = sh.off[cr][warp];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) pos += __popc(__ballot_sync(0xffffffffu, (m4 >> e) & 1u) & lt);
-        if (m4 == 0u) continue;
-        const int i = c * kTkRound + 4 * tid;
-        const uint4 k4 = get4(c);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (((m4 >> e) & 1u) && pos < (uint32_t)p.k)
-            emit(i + e, e == 0 ? k4.x : e == 1 ? k4.y : e == 2 ? k4.z : k4.w, pos);
-          pos += (m4 >> e) & 1u;
-        }
-      }
-      __syncthreads();  // the offsets are read before the next block rewrites them
-    }
-  }
-  const int cnt = (int)min(sh.base, (uint32_t)p.k);
-
-  if constexpr (!MERGE) {
-    for (int j = cnt + tid; j < p.k; j += kTkThreads) {
-      p.cand_score[li * p.k + j] = -INFINITY;
-      p.cand_idx[li * p.k + j] = -1;
-    }
-  } else {
-    // sorted[0, cnt) holds the selected entries in index order: shard d's list is the run
-    // of entries in [d * kin, (d + 1) * kin).  First the run boundaries, then the ids.
-    if (tid <= p.D) {
-      const int target = tid * p.stride;
-      int lo = 0, hi = cnt;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (sorted[mid] < target) lo = mid + 1; else hi = mid;
-      }
-      sh.run[tid] = lo;
-    }
-    if (tid == 0) sh.maxid = -1;
-    __syncthreads();
-    int mx = -1;
-    for (int j0 = tid; j0 < cnt; j0 += 4 * kTkThreads) {  // four id loads in flight
-      int id[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kTkThreads;
-        id[u] = j < cnt ? src.gid(sorted[j]) : -1;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = j0 + u * kTkThreads;
-        if (j < cnt) sorted[j] = id[u];
-        mx = max(mx, id[u]);
-      }
-    }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0 && mx >= 0) atomicMax(&sh.maxid, mx);
-    __syncthreads();
-    int32_t* out = p.topk + li * p.k;
-    // ids below 32 x the staging's words: a bitmap of the selected ids over the staging (free
-    // now) gives their increasing order directly -- each thread counts the set bits of its
-    // words, one scan, and writes its ids in order.  Not taken when an id repeats (another
-    // shard's list held it too): then the runs are merged as below.
-    const int nw = (sh.maxid >> 5) + 1;
-    if (runs_inside && sh.maxid >= 0 && nw <= p.stage) {
-      uint32_t* bm = keys;
-      for (int w = tid; w < nw; w += kTkThreads) bm[w] = 0u;
-      __syncthreads();
-      bool dup = false;
-      for (int j = tid; j < cnt; j += kTkThreads) {
-        const int id = sorted[j];
-        const uint32_t bit = 1u << (id & 31);
-        dup |= (atomicOr(&bm[id >> 5], bit) & bit) != 0u;
-      }
-      if (!__syncthreads_or(dup)) {
-        const int W = (nw + kTkThreads - 1) / kTkThreads;
-        const int w0 = min(tid * W, nw), w1 = min(w0 + W, nw);
-        uint32_t c = 0;
-        for (int w = w0; w < w1; ++w) c += __popc(bm[w]);
-        uint32_t total;
-        uint32_t pos = tk_scan(c, sh.ws, &total);
-        for (int w = w0; w < w1; ++w) {
-          uint32_t b = bm[w];
-          while (b != 0u) {
-            out[pos++] = 32 * w + __ffs(b) - 1;
-            b &= b - 1u;
-          }
-        }
-        for (int j = cnt + tid; j < p.k; j += kTkThreads) out[j] = -1;
-        if (tid == 0 && p.count) p.count[li] = cnt;
-        return;
-      }
-    }
-    // runs in increasing id order (as dcp_topk_local writes its lists): merged pairwise
-    bool unsorted = false;  // a pair inside a run out of order (pairs across runs may descend)
-    for (int j = tid; j + 1 < cnt; j += kTkThreads) {
-      int lo = 0, hi = p.D;  // the run of entry j + 1: the last d with run[d] <= j + 1
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (sh.run[mid] <= j + 1) lo = mid; else hi = mid - 1;
-      }
-      unsorted |= sh.run[lo] != j + 1 && sorted[j] >= sorted[j + 1];
-    }
-    if (!__syncthreads_or(unsorted)) {
-      // merge the runs pairwise, ceil(log2 D) levels between sorted[] and a second buffer,
-      // the last level into the output: each thread takes a slice of the output, finds
-      // where its pair's two runs stand at the slice start (a merge-path binary search) and
-      // merges sequentially from there
-      int32_t* src_b = sorted;
-      int32_t* dst_b = sorted2;
-      int nr = p.D;
-      const int E = (cnt + kTkThreads - 1) / kTkThreads;
-      if (nr == 1) {
-        for (int j = tid; j < cnt; j += kTkThreads) out[j] = src_b[j];
-      }
-      while (nr > 1) {
-        const bool last = nr <= 2;
-        const int np = (nr + 1) / 2;  // pairs; the last may hold one run
-        const int o0 = tid * E, o1 = min(cnt, o0 + E);
-        if (o0 < o1) {
-          int q = 0, hi = np - 1;  // the pair holding output o0: last q with run[2q] <= o0
-          while (q < hi) {
-            const int mid = (q + hi + 1) >> 1;
-            if (sh.run[2 * mid] <= o0) q = mid; else hi = mid - 1;
-          }
-          int ps = sh.run[2 * q], pm = sh.run[min(2 * q + 1, nr)], pe = sh.run[min(2 * q + 2, nr)];
-          const int d = o0 - ps;
-          int lo = max(0, d - (pe - pm)), up = min(d, pm - ps);
-          while (lo < up) {
-            const int mid = (lo + up) >> 1;
-            if (src_b[ps + mid] < src_b[pm + d - mid - 1]) lo = mid + 1; else up = mid;
-          }
-          int ia = ps + lo, ib = pm + d - lo;
-          for (int o = o0; o < o1; ++o) {
-            while (o == pe && q + 1 < np) {  // the slice runs on into the next (non-empty) pair
-              ++q;
-              ps = sh.run[2 * q];
-              pm = sh.run[min(2 * q + 1, nr)];
-              pe = sh.run[min(2 * q + 2, nr)];
-              ia = ps;
-              ib = pm;
-            }
-            const int v = (ib >= pe || (ia < pm && src_b[ia] < src_b[ib])) ? src_b[ia++] : src_b[ib++];
-            if (last) out[o] = v; else dst_b[o] = v;
-          }
-        }
-        __syncthreads();
-        if (tid == 0) {  // the merged runs' boundaries
-          for (int r = 0; r < np; ++r) sh.run[r] = sh.run[2 * r];
-          sh.run[np] = cnt;
-        }
-        __syncthreads();
-        int32_t* t = src_b;
-        src_b = dst_b;
-        dst_b = t;
-        nr = np;
-      }
-      for (int j = cnt + tid; j < p.k; j += kTkThreads) out[j] = -1;
-    } else {
-      // any order: bitonic sort over p.kp >= k entries
-      for (int j = cnt + tid; j < p.kp; j += kTkThreads) sorted[j] = INT_MAX;
-      __syncthreads();
-      for (int size = 2; size <= p.kp; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int t = tid; t < p.kp / 2; t += kTkThreads) {
-            const int i = 2 * t - (t & (stride - 1));
-            const int j = i + stride;
-            const int a = sorted[i], b = sorted[j];
-            if ((a > b) == ((i & size) == 0)) {
-              sorted[i] = b;
-              sorted[j] = a;
+              if ((h & msk_hi) == pre_hi) atomicAdd(&hist[(h >> shift) & wm], 1u);
+            } else if (h == pre_hi) {
+              const uint32_t l = ~(uint32_t)src.gid(i);
+              if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & wm], 1u);
             }
           }
           __syncthreads();
+          tk_find_bin_w0<kTkCandBins>(hist, krem, sh);
+          krem -= sh.above;
+          if (!lo) {
+            pre_hi |= sh.bin << shift;
+            msk_hi |= wm << shift;
+          } else {
+            pre_lo |= sh.bin << shift;
+            msk_lo |= wm << shift;
+          }
+          done = sh.binh == krem;  // (always by the last digit: keys differ)
+          // (the next digit's clear follows its reads of sh and of the histogram: warp 0 read
+          // the histogram before the barrier above, and sh is next written after two more)
+        }
+      } else {
+        wide = true;
+      }
+    }
+    if (search) {
+      // the further digits over every entry: lists past the staging, or too many candidates
+      for (int dg = 1; dg < 6 && wide && !done; ++dg) {
+        const bool lo = dg >= 3;
+        const int shift = dg % 3 == 1 ? 10 : dg % 3 == 2 ? 0 : 21;
+        const int nb = dg % 3 == 2 ? 1024 : 2048;
+        for (int i = tid; i < kTkBins; i += kTkThreads) hist[i] = 0u;
+        __syncthreads();
+        if (staged && !lo) {
+          // a high-word digit over the staged keys: compile-time shifts, one 16-B load per
+          // four keys, an atomic only for the keys still in play
+          for (int c = 0; c < rounds; ++c) {
+            const uint4 k4 = *reinterpret_cast<const uint4*>(keys + c * kTkRound + 4 * tid);
+            const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if ((h[e] & msk_hi) == pre_hi)
+                atomicAdd(&hist[dg == 1 ? (h[e] >> 10) & 2047u : h[e] & 1023u], 1u);
+          }
+        } else {
+          for (int c = 0; c < rounds; ++c) {
+            const uint4 k4 = get4(c);
+            const uint32_t h[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (!lo) {
+                hist_add(hist, h[e], msk_hi, pre_hi, shift, nb);
+              } else if (h[e] == pre_hi) {
+                const uint32_t l = ~(uint32_t)src.gid(c * kTkRound + 4 * tid + e);
+                if ((l & msk_lo) == pre_lo) atomicAdd(&hist[(l >> shift) & (nb - 1)], 1u);
+              }
+            }
+          }
+        }
+        __syncthreads();
+        if (nb == 2048)
+          tk_find_bin<2048 / kTkThreads>(hist, krem, sh);
+        else
+          tk_find_bin<1024 / kTkThreads>(hist, krem, sh);
+        krem -= sh.above;
+        if (!lo) {
+          pre_hi |= sh.bin << shift;
+          msk_hi |= (uint32_t)(nb - 1) << shift;
+        } else {
+          pre_lo |= sh.bin << shift;
+          msk_lo |= (uint32_t)(nb - 1) << shift;
+        }
+        done = sh.binh == krem;
+        __syncthreads();  // every thread has read the bin before the histogram is cleared
+      }
+    }
+    const uint32_t t_hi = pre_hi, t_lo = pre_lo;
+
+    auto selected = [&](uint32_t h, int i) -> bool {
+      return h != 0u && (h > t_hi || (h == t_hi && (t_lo == 0u || ~(uint32_t)src.gid(i) >= t_lo)));
+    };
+    const bool no_ties = t_lo == 0u;  // then the selection is key >= t_hi (t_hi >= 1)
+    // write selected entry i (with key h) at output position pos (< k)
+    auto emit = [&](int i, uint32_t h, uint32_t pos) {
+      if (MERGE) {
+        sorted[pos] = i;  // the entry; its id is loaded below, all at once
+      } else {
+        // the score from its key (exact; a zero is re-read, the key merges -0 and +0)
+        p.cand_score[li * p.k + pos] = h == 0x80000000u ? src.score(i) : key_score(h);
+        p.cand_idx[li * p.k + pos] = src.gid(i);
+      }
+    };
+    if (staged) {
+      // the candidates that reach T join the entries above the first digit's bin; then a
+      // stable compaction: one block scan of the counts, each thread's entries in order
+      for (uint32_t m = cmask; m != 0u; m &= m - 1u) {
+        const int b = __ffs(m) - 1;
+        if (selected(keys[e0 + b], e0 + b)) amask |= 1u << b;
+      }
+      uint32_t smask = amask;
+      uint32_t total;
+      uint32_t pos = tk_scan((uint32_t)__popc(smask), sh.ws, &total);
+      // candidate lists with k <= kTkBins: the selected entries' indices go to the histogram's
+      // words first, and are written out with consecutive threads on consecutive positions
+      const bool via_smem = !MERGE && p.k <= kTkBins;
+      int32_t* sel = reinterpret_cast<int32_t*>(hist);
+      while (smask != 0u && pos < (uint32_t)p.k) {
+        const int e = __ffs(smask) - 1;
+        smask &= smask - 1u;
+        const int i = e0 + e;
+        if (via_smem)
+          sel[pos++] = i;
+        else
+          emit(i, keys[i], pos++);
+      }
+      if (tid == 0) sh.base = total;
+      __syncthreads();
+      if (via_smem) {
+        const int ns = (int)min(total, (uint32_t)p.k);
+        for (int j = tid; j < ns; j += kTkThreads) {
+          const int i = sel[j];
+          emit(i, keys[i], (uint32_t)j);
         }
       }
-      for (int j = tid; j < p.k; j += kTkThreads) out[j] = j < cnt ? sorted[j] : -1;
+    } else {
+      // lists past the staging: the keys come from L2, in rounds; a block of kTkBlockRounds
+      // rounds at a time: count per (round, warp), one scan, then each warp writes its entries
+      // at positions found with ballots
+      auto sel4 = [&](const uint4& k4, int i) -> uint32_t {  // bit e: entry i + e is selected
+        if (no_ties)
+          return (uint32_t)(k4.x >= t_hi) | (uint32_t)(k4.y >= t_hi) << 1 |
+                 (uint32_t)(k4.z >= t_hi) << 2 | (uint32_t)(k4.w >= t_hi) << 3;
+        return (uint32_t)selected(k4.x, i) | (uint32_t)selected(k4.y, i + 1) << 1 |
+               (uint32_t)selected(k4.z, i + 2) << 2 | (uint32_t)selected(k4.w, i + 3) << 3;
+      };
+      if (tid == 0) sh.base = 0u;
+      for (int c0 = 0; c0 < rounds; c0 += kTkBlockRounds) {
+        const int nr = min(kTkBlockRounds, rounds - c0);
+        uint32_t selmask = 0;  // 4 bits per round of the block
+        for (int cr = 0; cr < nr; ++cr) {
+          const int c = c0 + cr;
+          const uint32_t m4 = sel4(get4(c), c * kTkRound + 4 * tid);
+          selmask |= m4 << (4 * cr);
+          const uint32_t wsum = __reduce_add_sync(0xffffffffu, (uint32_t)__popc(m4));
+          if (lane == 0) sh.cw[cr][warp] = wsum;
+        }
+        __syncthreads();
+        if (warp == 0) {  // exclusive scan of the block's (round, warp) counts in index order
+          const int per = kTkBlockRounds * kTkWarps / 32;
+          uint32_t v[kTkBlockRounds * kTkWarps / 32], run = 0;
+#pragma unroll
+          for (int j = 0; j < per; ++j) {
+            const int q = lane * per + j;
+            v[j] = q / kTkWarps < nr ? sh.cw[q / kTkWarps][q % kTkWarps] : 0u;
+            run += v[j];
+          }
+          uint32_t x = run;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+          }
+          uint32_t pos = sh.base + x - run;
+#pragma unroll
+          for (int j = 0; j < per; ++j) {
+            const int q = lane * per + j;
+            sh.off[q / kTkWarps][q % kTkWarps] = pos;
+            pos += v[j];
+          }
+          const uint32_t total = __shfl_sync(0xffffffffu, x, 31);
+          __syncwarp();
+          if (lane == 0) sh.base += total;
+        }
+        __syncthreads();
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int cr = 0; cr < nr; ++cr) {
+          const int c = c0 + cr;
+          const uint32_t m4 = (selmask >> (4 * cr)) & 15u;
+          // entries of lower lanes come first, then this lane's in order
+          uint32_t pos = sh.off[cr][warp];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pos += __popc(__ballot_sync(0xffffffffu, (m4 >> e) & 1u) & lt);
+          if (m4 == 0u) continue;
+          const int i = c * kTkRound + 4 * tid;
+          const uint4 k4 = get4(c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (((m4 >> e) & 1u) && pos < (uint32_t)p.k)
+              emit(i + e, e == 0 ? k4.x : e == 1 ? k4.y : e == 2 ? k4.z : k4.w, pos);
+            pos += (m4 >> e) & 1u;
+          }
+        }
+        __syncthreads();  // the offsets are read before the next block rewrites them
+      }
     }
-    if (tid == 0 && p.count) p.count[li] = cnt;
+    const int cnt = (int)min(sh.base, (uint32_t)p.k);
+
+    if constexpr (!MERGE) {
+      for (int j = cnt + tid; j < p.k; j += kTkThreads) {
+        p.cand_score[li * p.k + j] = -INFINITY;
+        p.cand_idx[li * p.k + j] = -1;
+      }
+    } else {
+      // sorted[0, cnt) holds the selected entries in index order: shard d's list is the run
+      // of entries in [d * kin, (d + 1) * kin).  First the run boundaries, then the ids.
+      if (tid <= p.D) {
+        const int target = tid * p.stride;
+        int lo = 0, hi = cnt;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (sorted[mid] < target) lo = mid + 1; else hi = mid;
+        }
+        sh.run[tid] = lo;
+      }
+      if (tid == 0) sh.maxid = -1;
+      __syncthreads();
+      int mx = -1;
+      bool pad = false;
+      for (int j0 = tid; j0 < cnt; j0 += 4 * kTkThreads) {  // four id loads in flight
+        int id[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * kTkThreads;
+          id[u] = j < cnt ? src.gid(sorted[j]) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * kTkThreads;
+          if (j < cnt) {
+            sorted[j] = id[u];
+            pad |= id[u] < 0;
+          }
+          mx = max(mx, id[u]);
+        }
+      }
+      if (__syncthreads_or(pad && !exact)) continue;  // a padding entry was selected
+      mx = __reduce_max_sync(0xffffffffu, mx);
+      if (lane == 0 && mx >= 0) atomicMax(&sh.maxid, mx);
+      __syncthreads();
+      int32_t* out = p.topk + li * p.k;
+      // ids below 32 x the staging's words: a bitmap of the selected ids over the staging (free
+      // now) gives their increasing order directly -- each thread counts the set bits of its
+      // words, one scan, and writes its ids in order.  Not taken when an id repeats (another
+      // shard's list held it too): then the runs are merged as below.
+      const int nw = (sh.maxid >> 5) + 1;
+      if (runs_inside && sh.maxid >= 0 && nw <= p.stage) {
+        uint32_t* bm = keys;
+        for (int w = tid; w < nw; w += kTkThreads) bm[w] = 0u;
+        __syncthreads();
+        bool dup = false;
+        for (int j = tid; j < cnt; j += kTkThreads) {
+          const int id = sorted[j];
+          const uint32_t bit = 1u << (id & 31);
+          dup |= (atomicOr(&bm[id >> 5], bit) & bit) != 0u;
+        }
+        if (!__syncthreads_or(dup)) {
+          const int W = (nw + kTkThreads - 1) / kTkThreads;
+          const int w0 = min(tid * W, nw), w1 = min(w0 + W, nw);
+          uint32_t c = 0;
+          for (int w = w0; w < w1; ++w) c += __popc(bm[w]);
+          uint32_t total;
+          uint32_t pos = tk_scan(c, sh.ws, &total);
+          for (int w = w0; w < w1; ++w) {
+            uint32_t b = bm[w];
+            while (b != 0u) {
+              out[pos++] = 32 * w + __ffs(b) - 1;
+              b &= b - 1u;
+            }
+          }
+          for (int j = cnt + tid; j < p.k; j += kTkThreads) out[j] = -1;
+          if (tid == 0 && p.count) p.count[li] = cnt;
+          return;
+        }
+      }
+      // runs in increasing id order (as dcp_topk_local writes its lists): merged pairwise
+      bool unsorted = false;  // a pair inside a run out of order (pairs across runs may descend)
+      for (int j = tid; j + 1 < cnt; j += kTkThreads) {
+        int lo = 0, hi = p.D;  // the run of entry j + 1: the last d with run[d] <= j + 1
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (sh.run[mid] <= j + 1) lo = mid; else hi = mid - 1;
+        }
+        unsorted |= sh.run[lo] != j + 1 && sorted[j] >= sorted[j + 1];
+      }
+      if (!__syncthreads_or(unsorted)) {
+        // merge the runs pairwise, ceil(log2 D) levels between sorted[] and a second buffer,
+        // the last level into the output: each thread takes a slice of the output, finds
+        // where its pair's two runs stand at the slice start (a merge-path binary search) and
+        // merges sequentially from there
+        int32_t* src_b = sorted;
+        int32_t* dst_b = sorted2;
+        int nr = p.D;
+        const int E = (cnt + kTkThreads - 1) / kTkThreads;
+        if (nr == 1) {
+          for (int j = tid; j < cnt; j += kTkThreads) out[j] = src_b[j];
+        }
+        while (nr > 1) {
+          const bool last = nr <= 2;
+          const int np = (nr + 1) / 2;  // pairs; the last may hold one run
+          const int o0 = tid * E, o1 = min(cnt, o0 + E);
+          if (o0 < o1) {
+            int q = 0, hi = np - 1;  // the pair holding output o0: last q with run[2q] <= o0
+            while (q < hi) {
+              const int mid = (q + hi + 1) >> 1;
+              if (sh.run[2 * mid] <= o0) q = mid; else hi = mid - 1;
+            }
+            int ps = sh.run[2 * q], pm = sh.run[min(2 * q + 1, nr)], pe = sh.run[min(2 * q + 2, nr)];
+            const int d = o0 - ps;
+            int lo = max(0, d - (pe - pm)), up = min(d, pm - ps);
+            while (lo < up) {
+              const int mid = (lo + up) >> 1;
+              if (src_b[ps + mid] < src_b[pm + d - mid - 1]) lo = mid + 1; else up = mid;
+            }
+            int ia = ps + lo, ib = pm + d - lo;
+            for (int o = o0; o < o1; ++o) {
+              while (o == pe && q + 1 < np) {  // the slice runs on into the next (non-empty) pair
+                ++q;
+                ps = sh.run[2 * q];
+                pm = sh.run[min(2 * q + 1, nr)];
+                pe = sh.run[min(2 * q + 2, nr)];
+                ia = ps;
+                ib = pm;
+              }
+              const int v = (ib >= pe || (ia < pm && src_b[ia] < src_b[ib])) ? src_b[ia++] : src_b[ib++];
+              if (last) out[o] = v; else dst_b[o] = v;
+            }
+          }
+          __syncthreads();
+          if (tid == 0) {  // the merged runs' boundaries
+            for (int r = 0; r < np; ++r) sh.run[r] = sh.run[2 * r];
+            sh.run[np] = cnt;
+          }
+          __syncthreads();
+          int32_t* t = src_b;
+          src_b = dst_b;
+          dst_b = t;
+          nr = np;
+        }
+        for (int j = cnt + tid; j < p.k; j += kTkThreads) out[j] = -1;
+      } else {
+        // any order: bitonic sort over p.kp >= k entries
+        for (int j = cnt + tid; j < p.kp; j += kTkThreads) sorted[j] = INT_MAX;
+        __syncthreads();
+        for (int size = 2; size <= p.kp; size <<= 1) {
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < p.kp / 2; t += kTkThreads) {
+              const int i = 2 * t - (t & (stride - 1));
+              const int j = i + stride;
+              const int a = sorted[i], b = sorted[j];
+              if ((a > b) == ((i & size) == 0)) {
+                sorted[i] = b;
+                sorted[j] = a;
+              }
+            }
+            __syncthreads();
+          }
+        }
+        for (int j = tid; j < p.k; j += kTkThreads) out[j] = j < cnt ? sorted[j] : -1;
+      }
+      if (tid == 0 && p.count) p.count[li] = cnt;
+    }
+    return;
   }
 }
 
