@@ -170,6 +170,26 @@ def test_local_then_merge_is_the_unsharded_topk(dcp, D, I, k):
     assert np.array_equal(top.cpu().numpy(), wt) and np.array_equal(cnt.cpu().numpy(), wc)
 
 
+def test_merge_padding_with_the_highest_scores(dcp):
+    """Padding entries (id -1) carrying the largest scores: a selection by score alone would
+    take them, so the merge must select again with the ids; rows without such padding keep
+    the score-only selection.  Both against the oracle."""
+    D, R, kin, k = 8, 4, 2048, 2048
+    rng = np.random.default_rng(11)
+    ids = np.stack([rng.permutation(D * kin * 2)[:D * kin].reshape(D, kin) for _ in range(R)], 1)
+    ids = np.sort(ids, axis=2).astype(np.int32)
+    sc = rng.standard_normal((D, R, kin)).astype(np.float32)
+    pad = rng.random(ids.shape) < 0.05
+    pad[:, 1, :] = False  # row 1: no padding
+    ids[pad] = -1
+    sc[pad] = 50.0        # above every real score
+    sc[:, 2, :][pad[:, 2, :]] = -np.inf  # row 2: padding as the local lists write it
+    top, cnt = dcp.dcp_topk_merge(torch.from_numpy(sc).to(dev), torch.from_numpy(ids).to(dev), k)
+    torch.cuda.synchronize()
+    wt, wc = otk.merge_topk(sc, ids, k)
+    assert np.array_equal(top.cpu().numpy(), wt) and np.array_equal(cnt.cpu().numpy(), wc)
+
+
 def test_infinities_and_signed_zeros(dcp):
     """+inf ranks above every finite score, -inf and NaN are never candidates, -0 ranks as
     +0 (ties by slot), through both kernels; aligned rows of 6000 and unaligned ones of
