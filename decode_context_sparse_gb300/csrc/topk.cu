@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kTkThreads, 3) topk_kernel(const TopkParams p)
     const bool exact = !MERGE || attempt > 0;
     const bool masync = MERGE && !exact && staged && src.vec;
     if (masync) {  // the scores, every piece at once (n is a multiple of 4)
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < kTkBlockRounds; ++c) {
         const int i = c * kTkRound + 4 * tid;
         if (i < n) cp_async16(keys + i, src.sc + src.off(i));
