@@ -130,6 +130,7 @@ struct TcShared {
   uint64_t self_full[2], self_free[2];  // stage A -> stage B hand-over of this CTA's partial
   uint64_t s_free[2];                   // stage A has read a logit buffer out of TMEM
   uint64_t bx_full[4][2], bl_full[4];   // stage B pairs: partial row maxima / row sums posted
+  uint64_t ep_done[4];                  // stage B pairs: a tiled-store epilogue's staging free
   float bx[2][2][128];                  // [half][tile parity][head] partial row max of a tile
   float bl[2][128];                     // [half][head] partial row sum of a unit
   uint32_t stg_mask[4];
@@ -310,7 +311,8 @@ __device__ __noinline__ float tc_load_q(const uint4* __restrict__ src, bool vali
 template <int KVT, bool FUSED, bool SPARSE>
 __global__ void __launch_bounds__(kTcThreads, 1)
 decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_lat,
-                 const __grid_constant__ CUtensorMap tm_tail) {
+                 const __grid_constant__ CUtensorMap tm_tail,
+                 const __grid_constant__ CUtensorMap tm_out) {
   using C = TcCfg<KVT>;
   using L = TcLay<KVT>;
   constexpr int TN = kTN, NS = C::NS, NK = C::NK;
@@ -363,6 +365,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
       mbar_init(&sh.bx_full[g][0], 2);
       mbar_init(&sh.bx_full[g][1], 2);
       mbar_init(&sh.bl_full[g], 2);
+      mbar_init(&sh.ep_done[g], 2);
     }
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -935,6 +938,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     bool from_start = sh.tile0 == 0;
     int slot_idx = 0;             // workspace slot of a split unit: 0 first unit, 1 last
     int nunit = 0;                // units finished (parity of the row-sum exchange)
+    int nep = 0;                  // tiled-store epilogues done (phase of ep_done)
     bool ok = true;
 
     // Finish the current unit: normalise and write this half's O columns (or a split
@@ -982,6 +986,27 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
                    make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]));
           continue;
         }
+        if (!FUSED && p.tma_out) {
+          // this warp's 32 rows x 32 columns, as the output map's 128-B swizzled box, in its
+          // rows of the P buffer of its half (free: see the barrier after the rounds), then
+          // one tiled store by lane 0; the previous round's store must have read the box
+          unsigned char* box = smem + L::OFF_P + half * L::P_BYTES + grp * 4096;
+          if (rc > 0) {
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(box + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_float4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && grp * 32 < H) {
+            tma_store_3d(&tm_out, box, (int)crank * 256 + 16 * c0, grp * 32, (int)u);
+            bulk_commit();
+          }
+          continue;
+        }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           *reinterpret_cast<float4*>(stage_addr(h, k)) =
@@ -1013,6 +1038,15 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
         __syncwarp();  // the rows are read before the next round overwrites them
       }
       tc_fence_before();
+      if (!FUSED && complete && p.tma_out) {
+        // both halves' boxes read out (each half stages in the P buffer whose other columns
+        // the other half may fill with the next tile's P) before either half goes on
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.ep_done[grp]);
+        if (!(ok = mbar_wait(&sh.ep_done[grp], nep & 1, abort_flag))) return;
+        ++nep;
+      }
       if (complete) {
         if (half == 0 && crank == 0 && h < H) p.lse[u * H + h] = lse_v;
         return;
@@ -1180,6 +1214,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     // the range ended inside a unit (Walk.next does not move past the last tile):
     // publish that unit's partial
     if (ok && j == ntiles && ntiles > 0 && w.lt != w.info.ntile - 1) finish_unit(ntiles - 1, false);
+    if (!FUSED && lane == 0) bulk_wait0();  // this warp's tiled stores complete
   }
 
   // ---------------------------------------------------------------- teardown
@@ -1356,15 +1391,33 @@ static cudaError_t make_pool_maps(const DecodeParams& p, int kv_dtype, CUtensorM
   return cudaSuccess;
 }
 
+// The partial form's output as a 3-D tensor [units][heads][512] fp32 with 32 x 32 boxes in the
+// 128-B swizzle; only for a 16-B aligned output (else the kernel stores rows itself).
+static bool make_out_map(const DecodeParams& p, CUtensorMap* out) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr || (reinterpret_cast<uintptr_t>(p.out) & 15) != 0 || p.num_units < 1)
+    return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kDv, (cuuint64_t)p.heads, (cuuint64_t)p.num_units};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDv * 4, (cuuint64_t)p.heads * kDv * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.out, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int KVT, bool FUSED, bool SPARSE>
-static cudaError_t tc_launch_one(const DecodeParams& p, cudaStream_t st) {
+static cudaError_t tc_launch_one(const DecodeParams& p0, cudaStream_t st) {
   auto kern = decode_tc_kernel<KVT, FUSED, SPARSE>;
   const int smem = TcLay<KVT>::SMEM;
   cudaError_t e = raise_smem_limit((const void*)kern, smem);
   if (e != cudaSuccess) return e;
-  alignas(64) CUtensorMap lat, tail;
-  e = make_pool_maps(p, KVT, &lat, &tail);
+  alignas(64) CUtensorMap lat, tail, outm;
+  e = make_pool_maps(p0, KVT, &lat, &tail);
   if (e != cudaSuccess) return e;
+  DecodeParams p = p0;
+  memset(&outm, 0, sizeof(outm));
+  p.tma_out = !FUSED && make_out_map(p, &outm) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * p.pairs, 1, 1);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
@@ -1377,7 +1430,7 @@ static cudaError_t tc_launch_one(const DecodeParams& p, cudaStream_t st) {
   attrs[0].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, p, lat, tail);
+  e = cudaLaunchKernelEx(&cfg, kern, p, lat, tail, outm);
   if (e != cudaSuccess || p.pairs < 2) return e;
   tc_split_merge_kernel<FUSED><<<p.pairs * 2 * 32, 128, 0, st>>>(p);
   return cudaGetLastError();

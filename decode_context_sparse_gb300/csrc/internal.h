@@ -46,6 +46,7 @@ struct DecodeParams {
   float* tc_l;            // their LSEs [pairs][2][2][128]
   int64_t* tc_desc;       // [T, pairs owning tiles] + per (pair, slot) (unit, first tile, end tile)
   int32_t* err_timeout;   // error word for bounded-wait timeouts (whenever given)
+  int tma_out;            // partial: finished units' rows go out by tiled stores (set at launch)
 };
 
 // Per-device facts (csrc/device.cu): the SM count of the current device, and raising a

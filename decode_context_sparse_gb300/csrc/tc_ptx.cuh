@@ -312,6 +312,14 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int x, 
       "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
       : "memory");
 }
+// Tiled store of a shared-memory box (1024-B aligned for a swizzled map) to the 3-D tensor
+// `tmap` at element coordinates (x, y, z), as a bulk group of this thread; parts of the box
+// outside the tensor are not written.  x * element size must be a multiple of 16 B.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+                   "l"(tmap), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
