@@ -225,7 +225,7 @@ typedef struct {
                                   grid and the workspace); sparse: ignored */
   /* outputs */
   void* out;                   /* (device) partial: [num_shards][rows][heads][512] fp32;
-                                  fused: [rows][heads][512] bf16 */
+                                  fused: [rows][heads][512] bf16; 16-B aligned */
   float* lse;                  /* (device) partial: [num_shards][rows][heads];
                                   fused: [rows][heads]; natural log; -inf = no KV */
   /* scratch */

@@ -49,6 +49,30 @@ def test_both_paths_match_oracle(dcp, path, kv):
     check_lse(pl[2], sl, path + " partial lse")
 
 
+@pytest.mark.parametrize("heads", [128, 48])
+def test_partial_every_shard_and_output_alignment(dcp, heads):
+    """The tensor-core partial decode writes a finished unit's rows by tiled stores: every
+    shard's output and LSE match the oracle, also with 48 heads (a head group's box partly
+    outside the tensor).  An output that is not 16-B aligned is refused."""
+    prob = synth.make_decode_problem("align", [2600, 900], heads, 700, synth.KV_FP8, 4, 1, mtp=2,
+                                     seed=83)
+    g = prob.to(DEV)
+    D = g.dcp
+    R = g.q.shape[0]
+    loc, cnt = dcp.dcp_remap_topk(g.topk, D, g.interleave)
+    args = (g.q, g.pool, g.kv_dtype, g.block_table, g.row_seq, g.sm_scale)
+    po, pl = dcp.mla_decode_partial_lse(*args, idx=loc, count=cnt, num_shards=D)
+    torch.cuda.synchronize()
+    for s in range(D):
+        so, sl = oracle.attention_problem(prob, shard=s)
+        check_out(po[s], so, "partial out shard %d" % s)
+        check_lse(pl[s], sl, "partial lse shard %d" % s)
+    buf = torch.zeros(D * R * heads * 512 + 1, dtype=torch.float32, device=DEV)
+    off = buf[1:].view(D, R, heads, 512)
+    with pytest.raises(dcp.DcpError):
+        dcp.mla_decode_partial_lse(*args, idx=loc, count=cnt, num_shards=D, out=off)
+
+
 def test_tc_timeout_flag_stays_clear(dcp):
     prob = synth.make_decode_problem("flag", [5000], 128, 2048, synth.KV_FP8, 8, 1, mtp=2, seed=82).to(DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
