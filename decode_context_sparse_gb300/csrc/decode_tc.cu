@@ -258,25 +258,31 @@ __device__ __forceinline__ uint32_t fp8_block_mul(float s) {
 // (two per column, at taddr), its 32 RoPE dims into row h of the SW128 A-operand tile qr.
 // The values are multiplied by 2^(14 - e), e the exponent of their largest magnitude (exact;
 // keeps them in FP16's range); returns 2^(e - 14), the factor that undoes it on the logits.
-// Two passes over the 36 16-B pieces (the largest magnitude, then the conversion), each
-// with twelve or eight loads in flight.  Not inlined: it runs once per row, and the warps
-// that call it keep their registers for the per-tile work.
-__device__ __noinline__ float tc_load_q(const uint4* __restrict__ src, bool valid, int crank,
-                                        uint32_t taddr, unsigned char* qr, int hrow) {
-  uint32_t mx = 0;  // largest |bf16| bit pattern over the CTA's 288 dims
-  if (valid) {
-#pragma unroll 12
-    for (int i = 0; i < 36; ++i) {
-      const uint4 v = __ldg(src + (i < 32 ? crank * 32 + i : 64 + crank * 4 + (i - 32)));
-      const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
-                             v.w & 0x7fff7fffu};
+// qs_prev is that factor of this head's previous row (0: none), whose e serves as a hint.
+// Without a hint: two passes over the 36 16-B pieces (the largest magnitude, then the
+// conversion).  With one (for the whole warp), one pass converts with it and finds the
+// largest magnitude on the way; any e from the true one - 8 to the true one + 1 gives the
+// same FP16 values up to the rounding of values 2^-20 below the largest, and none
+// overflows, so only a hint outside that range makes the warp convert again with the true
+// exponent.  Twelve or eight loads in flight.  Not inlined: it runs once per row, and the
+// warps that call it keep their registers for the per-tile work.
+constexpr int kNoQHint = -1000;
+
+__device__ __forceinline__ uint32_t q_piece_mx(const uint4& v, uint32_t mx) {
+  const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
+                         v.w & 0x7fff7fffu};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
-    }
-  }
-  const int e = (int)(mx >> 7) - 127;  // exponent of the largest magnitude
-  const bool zero = mx == 0 || e > 127 - 14;
-  const float up = zero ? 1.0f : __uint_as_float((uint32_t)(127 + 14 - e) << 23);
+  for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0xffffu, w[k] >> 16));
+  return mx;
+}
+
+// The conversion pass with exponent e; returns the largest |bf16| bit pattern it loaded.
+__device__ __forceinline__ uint32_t tc_q_convert(const uint4* __restrict__ src, bool valid,
+                                                 int crank, uint32_t taddr, unsigned char* qr,
+                                                 int hrow, int e) {
+  const bool noscale = e > 127 - 14;
+  const float up = noscale ? 1.0f : __uint_as_float((uint32_t)(127 + 14 - e) << 23);
+  uint32_t mx = 0;
 #pragma unroll 1
   for (int c = 0; c < 8; c += 2) {
     uint4 v[8];
@@ -289,6 +295,7 @@ __device__ __noinline__ float tc_load_q(const uint4* __restrict__ src, bool vali
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 u = v[4 * cc + i];
+        mx = q_piece_mx(u, mx);
         w[4 * i] = bf16x2_to_f16x2_mul(u.x, up);
         w[4 * i + 1] = bf16x2_to_f16x2_mul(u.y, up);
         w[4 * i + 2] = bf16x2_to_f16x2_mul(u.z, up);
@@ -300,12 +307,41 @@ __device__ __noinline__ float tc_load_q(const uint4* __restrict__ src, bool vali
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint4 v = valid ? __ldg(src + 64 + crank * 4 + i) : make_uint4(0u, 0u, 0u, 0u);
+    mx = q_piece_mx(v, mx);
     v = make_uint4(bf16x2_to_f16x2_mul(v.x, up), bf16x2_to_f16x2_mul(v.y, up),
                    bf16x2_to_f16x2_mul(v.z, up), bf16x2_to_f16x2_mul(v.w, up));
     *reinterpret_cast<uint4*>(qr + ((i ^ (hrow & 7)) << 4)) = v;
   }
   tmem_st_wait();
-  return zero ? 1.0f : __uint_as_float((uint32_t)(127 - 14 + e) << 23);
+  return mx;
+}
+
+__device__ __noinline__ float tc_load_q(const uint4* __restrict__ src, bool valid, int crank,
+                                        uint32_t taddr, unsigned char* qr, int hrow,
+                                        float qs_prev) {
+  const int e_hint =
+      qs_prev == 0.0f ? kNoQHint : (int)((__float_as_uint(qs_prev) >> 23) & 255u) - 127 + 14;
+  int e;
+  if (__all_sync(0xffffffffu, e_hint != kNoQHint)) {
+    e = e_hint;
+    const uint32_t mx = tc_q_convert(src, valid, crank, taddr, qr, hrow, e);
+    const int et = (int)(mx >> 7) - 127;
+    const bool redo = valid && mx != 0 && (et > e + 1 || et < e - 8);
+    if (__any_sync(0xffffffffu, redo)) {
+      if (mx != 0) e = et;
+      tc_q_convert(src, valid, crank, taddr, qr, hrow, e);
+    }
+  } else {
+    uint32_t mx = 0;  // largest |bf16| bit pattern over the CTA's 288 dims
+    if (valid) {
+#pragma unroll 12
+      for (int i = 0; i < 36; ++i)
+        mx = q_piece_mx(__ldg(src + (i < 32 ? crank * 32 + i : 64 + crank * 4 + (i - 32))), mx);
+    }
+    e = mx == 0 ? 127 : (int)(mx >> 7) - 127;  // (an all-zero head: no scaling)
+    tc_q_convert(src, valid, crank, taddr, qr, hrow, e);
+  }
+  return e > 127 - 14 ? 1.0f : __uint_as_float((uint32_t)(127 - 14 + e) << 23);
 }
 
 template <int KVT, bool FUSED, bool SPARSE>
@@ -789,12 +825,12 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_la
     const uint32_t trow = tbase + ((uint32_t)((warp & 3) * 32) << 16);
     float* xin = reinterpret_cast<float*>(smem + L::OFF_X);
     float* xself = reinterpret_cast<float*>(smem + L::OFF_SELF);
-    float qs = 1.0f;  // 2^(e - 14) of this head's Q in the current row (see tc_load_q)
+    float qs = 0.0f;  // 2^(e - 14) of this head's Q in the current row (see tc_load_q)
     auto load_q = [&](int64_t r) {
       const uint4* src = reinterpret_cast<const uint4*>(
           reinterpret_cast<const __nv_bfloat16*>(p.q) + (r * H + h) * kDqk);
       unsigned char* qr = smem + L::OFF_QR + (h >> 3) * 1024 + (h & 7) * 128;
-      qs = tc_load_q(src, h < H, (int)crank, trow + kColQ, qr, h);
+      qs = tc_load_q(src, h < H, (int)crank, trow + kColQ, qr, h, qs);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
