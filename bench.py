@@ -119,7 +119,7 @@ def dist_env():
 # DRAM traffic of the decode kernel (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of a 96-row slice of this workload (bench.py --seqs 16), per decode row; the bench
 # scales it to the full launch by rows, since the traffic grows with the rows processed.
-TRAFFIC_CAPTURE = {"bytes_per_row": (167.925504e6 + 18.008064e6) / 96, "rows": 96,
+TRAFFIC_CAPTURE = {"bytes_per_row": (168.456448e6 + 18.000896e6) / 96, "rows": 96,
                    "kernel": "decode_tc_kernel<FP8, fused, sparse>"}
 
 
